@@ -1,0 +1,72 @@
+"""Plants plausible mistakes in a copy of the oracle's C source (on the CPU)
+and checks that the pins reject every one: a pin that a dropped term, a wrong
+sign, a swapped index or a reversed tie rule would pass is no pin."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+from w4a16_group_quantized_moe_gb300 import inputs
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+
+# (name, original text, mutated text); each original must occur exactly once
+MUTANTS = [
+    ("nibble order reversed", "(qweight[qword] >> (4 * (kk % 8)))",
+     "(qweight[qword] >> (4 * (7 - kk % 8)))"),
+    ("zero nibble taken by column", "(qzeros[zword] >> (4 * (n % 8)))",
+     "(qzeros[zword] >> (4 * (kk % 8)))"),
+    ("zero point sign flipped", "return (double)(q - z) * s;", "return (double)(q + z) * s;"),
+    ("scale of group 0 everywhere", "scales[((size_t)e * N + n) * G + kk / 32]",
+     "scales[((size_t)e * N + n) * G]"),
+    ("gate used for up", "u += xv * oracle_dequant(w13q, w13s, w13z, 2 * I, H, e, I + i, kk);",
+     "u += xv * oracle_dequant(w13q, w13s, w13z, 2 * I, H, e, i, kk);"),
+    ("silu dropped", "hrow[i] = silu(g) * u;", "hrow[i] = g * u;"),
+    ("silu sign", "return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    ("no renormalisation", "topk_w[(size_t)t * k + j] = prob[e] / selected_mass;",
+     "topk_w[(size_t)t * k + j] = prob[e];"),
+    ("tie goes to higher index", "return a < b;", "return a > b;"),
+    ("combine weight dropped", "acc += topk_w[(size_t)t * k + j] * y[(size_t)r * H + n];",
+     "acc += y[(size_t)r * H + n];"),
+    ("segment order reversed", "for (int p = 0; p < P; ++p)\n            if (topk_ids[p] == e)",
+     "for (int p = P - 1; p >= 0; --p)\n            if (topk_ids[p] == e)"),
+    ("last group of K dropped", "for (int kk = 0; kk < H; ++kk) {",
+     "for (int kk = 0; kk < H - 32; ++kk) {"),
+]
+
+CHECKS = [
+    pins.test_dequant_unpacks_hand_derived_words,
+    pins.test_route_hand_derived_cases,
+    lambda m: pins.test_route_matches_brute_force_sort(m, 7, 512, 10),
+    lambda m: pins.test_align_matches_bincount_cumsum_and_stable_sort(m, 300, 64, 6),
+    lambda m: pins.test_layer_matches_dense_brute_force(m, pins.SHAPES[0]),
+    lambda m: pins.test_layer_matches_dense_brute_force(m, pins.SHAPES[1]),
+    pins.test_layer_constant_closed_form,
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, orig, mut):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor for '{name}' not unique"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(orig, mut))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-fvisibility=hidden", str(mpath), "-o", str(lib), "-lm"])
+    caught = []
+    with oracle.using_library(str(lib)):
+        for check in CHECKS:
+            try:
+                check(oracle)
+            except AssertionError:
+                caught.append(check)
+    assert caught, f"no pin rejects the planted mistake '{name}'"
+
+
+def test_unmutated_source_passes_every_check():
+    for check in CHECKS:
+        check(oracle)
+    assert inputs.TINY.shape.k == 2
