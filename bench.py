@@ -1,0 +1,366 @@
+"""Benchmark of the W4A16 group-32 MoE layer (libmoe_w4a16) on GB300.
+
+One step = the whole layer (route, align, gate_up+SiLU, down+combine: four C
+calls on one stream) over one batch of synthetic inputs already resident in
+HBM.  Default workload: Qwen4Exp-geometry decode, 1 token (hidden 2560,
+intermediate 640, 512 experts, top-10, W4A16 g32).
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every step L2
+is flushed by writing a 1 GiB buffer (outside the timed interval) and the
+router logits rotate over 32 pre-generated sets so the active experts change
+from step to step.  Each step is bracketed by CUDA events on the launching
+stream, with events around the gate/up kernel for the roofline line.  The
+flush kernel also keeps the GPU busy while the host enqueues the step, so
+host launch overhead does not show up inside the events.
+
+Multi-GPU: the layer has no cross-token exchange, so N GPUs run N independent
+replicas (weak scaling); value = all ranks' tokens / max-over-ranks time.
+
+--impl reference times the CPU oracle (the only other implementation there
+is) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s + achieved HBM GB/s (decode 1-8 tok), W4A16 g32, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen4exp_decode_T1_H2560_I640_E512_k10")
+    ap.add_argument("--sets", type=int, default=32)
+    ap.add_argument("--flush-mb", type=int, default=1024)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+            if hbm:
+                return float(hbm), "measured", d
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback", None
+
+
+def active_bytes(A: int, T: int, k: int, H: int, I: int):
+    """Algorithmic bytes of one layer step and of the gate/up launch."""
+    from w4a16_group_quantized_moe_gb300 import inputs
+    b = inputs.bytes_per_expert(H, I)
+    P = T * k
+    E_meta = 0
+    gate_up = A * b["w13"] + T * H * 2 + P * I * 2
+    layer = A * (b["w13"] + b["w2"]) + T * H * 2 * 2 + P * I * 2 * 2 + E_meta
+    return layer, gate_up
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_rate(wl, seconds: float, sets: int):
+    """Tokens/s of the CPU oracle (one thread) on a bounded sample: whole
+    layers over successive router-logit sets of the workload until `seconds`
+    of CPU work have been done."""
+    import oracle
+    from w4a16_group_quantized_moe_gb300 import inputs
+    sh = wl.shape
+    w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
+    tokens = 0
+    t0 = time.perf_counter()
+    s = 0
+    while True:
+        logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + s % sets,
+                                            wl.hot_experts, wl.hot_bias)
+        oracle.moe_forward(logits, x, w13, w2, sh.k)
+        tokens += sh.T
+        s += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return tokens / el, tokens, el, s
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    budget = 60.0
+    import oracle
+    from w4a16_group_quantized_moe_gb300 import inputs
+    oracle.build()
+    sh = wl.shape
+    w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
+    times = []
+    t_start = time.perf_counter()
+    for s in range(args.warmup + args.steps):
+        logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + s % args.sets,
+                                            wl.hot_experts, wl.hot_bias)
+        t0 = time.perf_counter()
+        oracle.moe_forward(logits, x, w13, w2, sh.k)
+        if s >= min(args.warmup, 1):
+            times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget and len(times) >= 3:
+            break
+    steps = len(times)
+    tot = sum(times)
+    value = sh.T * steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": min(args.warmup, 1),
+        "ms_per_step": 1e3 * tot / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "parallelism": "cpu, 1 thread"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} whole-layer steps of {wl.name} (T={sh.T}), "
+                                   f"router logits rotated over {args.sets} sets; run capped "
+                                   f"at {budget:.0f} s of CPU time (requested {args.steps})"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    from w4a16_group_quantized_moe_gb300 import inputs
+    wl = inputs.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import w4a16_group_quantized_moe_gb300 as moe
+
+    sh = wl.shape
+    T, H, I, E, k = sh.T, sh.H, sh.I, sh.E, sh.k
+    w13, w2 = inputs.make_weights(E, H, I, wl.seed)
+    dw13, dw2 = moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev)
+    del w13, w2
+    layer = moe.MoELayer(dw13, dw2, T, k, device=dev)
+    sets = []
+    for s in range(args.sets):
+        lg, xx = inputs.make_activations(T, H, E, wl.seed + 1000 + s, wl.hot_experts, wl.hot_bias)
+        sets.append((torch.from_numpy(lg).to(dev), torch.from_numpy(xx).to(dev)))
+    logits_buf = torch.empty((T, E), dtype=torch.float32, device=dev)
+    x_buf = torch.empty((T, H), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    route, align, gate_up, down = layer.bind(logits_buf, x_buf, stream)
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+
+    # active-expert count of every logits set (for the algorithmic bytes)
+    A_of = []
+    for lg, xx in sets:
+        logits_buf.copy_(lg)
+        x_buf.copy_(xx)
+        route(); align()
+        A_of.append(int(layer.meta[3].item()))
+
+    def step(s, ev=None):
+        lg, xx = sets[s % len(sets)]
+        logits_buf.copy_(lg, non_blocking=True)
+        x_buf.copy_(xx, non_blocking=True)
+        flush.fill_(s & 0xFF)
+        if ev is not None:
+            ev[0].record(stream)
+        route(); align()
+        if ev is not None:
+            ev[1].record(stream)
+        gate_up()
+        if ev is not None:
+            ev[2].record(stream)
+        down()
+        if ev is not None:
+            ev[3].record(stream)
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+    if moe.moe_get_device_error(layer.workspace):
+        raise RuntimeError("device error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for s in range(args.steps):
+            step(args.warmup + s, evs[s])
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    layer_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
+    gu_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
+    A_steps = np.array([A_of[(args.warmup + s) % len(sets)] for s in range(args.steps)])
+    flag = moe.moe_get_device_error(layer.workspace)
+    if flag:
+        raise RuntimeError(f"device error word 0x{flag:x} during timed steps")
+
+    tot_ms = float(layer_ms.sum())
+    if world > 1:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    value = world * T * args.steps / (tot_ms / 1e3)
+
+    lb, gb = zip(*(active_bytes(int(a), T, k, H, I) for a in A_steps))
+    layer_gbs = float(np.sum(lb) / (layer_ms.sum() / 1e3) / 1e9)
+    gu_gbs = float(np.sum(gb) / (gu_ms.sum() / 1e3) / 1e9)
+    peak, peak_kind, _ = peaks()
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # inputs from pinned memory, the four calls, D2H of the output
+    h_logits = [lg.cpu().pin_memory() for lg, _ in sets]
+    h_x = [xx.cpu().pin_memory() for _, xx in sets]
+    h_out = torch.empty((T, H), dtype=torch.float16).pin_memory()
+    e2e_steps = min(args.steps, 2000)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
+    for s in range(e2e_steps):
+        i = s % len(sets)
+        flush.fill_(s & 0xFF)
+        e2e_ev[s][0].record(stream)
+        logits_buf.copy_(h_logits[i], non_blocking=True)
+        x_buf.copy_(h_x[i], non_blocking=True)
+        route(); align(); gate_up(); down()
+        h_out.copy_(layer.out, non_blocking=True)
+        e2e_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev)
+    e2e_val = T * e2e_steps / (e2e_ms / 1e3)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_val = world * T * e2e_steps / (float(t.item()) / 1e3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, toks, el, n = cpu_oracle_rate(wl, args.cpu_seconds, args.sets)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole-layer steps ({toks} tokens) of {wl.name} over "
+                         f"{el:.1f} s, single-threaded fp64 C oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16", "data": "synthetic",
+            "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
+                       "group_size": 32, "parallelism": f"replicas x{world}",
+                       "l2": f"flushed before every timed step ({args.flush_mb} MiB write); "
+                             f"router logits rotated over {args.sets} sets",
+                       "mean_active_experts": float(A_steps.mean())},
+            "layer_hbm_gbs": layer_gbs,
+            "layer_us": {"median": float(np.median(layer_ms) * 1e3),
+                         "p10": float(np.percentile(layer_ms, 10) * 1e3),
+                         "p90": float(np.percentile(layer_ms, 90) * 1e3)},
+            "roofline": {"kernel": "moe_w4a16_gate_up_silu (stream_kernel<gate_up>)",
+                         "bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gu_gbs / peak, "peak_source": peak_kind,
+                         "gate_up_us_median": float(np.median(gu_ms) * 1e3),
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * E * 4 + T * H * 2,
+                    "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
+            "gpu_launches": (4 + (T > 8)) * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

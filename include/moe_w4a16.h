@@ -1,0 +1,175 @@
+/*
+ * moe_w4a16.h -- C ABI of libmoe_w4a16: the routed-expert MoE layer with
+ * W4A16 group-32 expert weights, as hand-written CUDA kernels for GB300
+ * (sm_103a).
+ *
+ * The layer (geometry from "[Model][SM70] Adapt Qwen3.8 Flash Next NVFP4",
+ * section Implemented route: hidden 2560, expert intermediate 640, 512
+ * experts, top-10; grouping and quantisation from "[Perf][SM70] Narrow
+ * Qwen3.8 AWQ active grouped decode", section Purpose: AWQ W4A16 "effective
+ * g32", "multi-row active-expert segments and offsets-based scheduling") is
+ * four calls, issued in this order on one stream:
+ *
+ *   moe_topk_route          logits -> top-k expert ids and renormalised weights
+ *   moe_align_offsets       ids -> per-expert segments of token-expert pairs
+ *   moe_w4a16_gate_up_silu  x, W13 -> h = silu(x Wg^T) * (x Wu^T), per pair
+ *   moe_w4a16_down_combine  h, W2, weights -> out = sum_j w_j * (h_j W2^T)
+ *
+ * Conventions for every call below.
+ *   - Pointers are CUDA device pointers unless marked (host).  Every device
+ *     pointer must be 16-byte aligned (PyTorch and cudaMalloc allocations
+ *     are); a misaligned pointer is rejected with MOE_ERR_INVALID_ARG.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: they validate arguments on the host,
+ *     enqueue kernels and return.  They never synchronise, never allocate
+ *     device or pinned memory, and never abort or trap.
+ *   - The caller owns every buffer.  The library keeps no state between
+ *     calls except cached device attributes (SM count, shared-memory limit).
+ *   - fp16 buffers hold IEEE binary16 values (passed as uint16_t*).
+ *   - T = tokens, E = experts, k = experts per token, H = hidden size,
+ *     I = expert intermediate size, P = T*k token-expert pairs.  A pair is
+ *     p = t*k + j: token t's j-th selected expert.
+ *   - Supported sizes: 0 <= T, 1 <= k <= min(E, 32), E <= 1024,
+ *     H and I positive multiples of 32, group_size == 32.  Anything else is
+ *     MOE_ERR_INVALID_ARG (malformed) or MOE_ERR_UNSUPPORTED (outside the
+ *     sizes above).  T == 0 is a no-op that returns MOE_OK.
+ *
+ * Packed weight layout (AWQ-style W4A16, groups of 32 along the reduction
+ * dimension K; row-major, little-endian 32-bit words).  For one expert's
+ * matrix W[N][K]:
+ *   qweight u32 [N][K/8]   : code of (n, kk) = bits 4*(kk%8)..+3 of word [n][kk/8]
+ *   scales  f16 [N][K/32]  : s of (n, kk) = scales[n][kk/32]
+ *   qzeros  u32 [N/8][K/32]: zero of (n, kk) = bits 4*(n%8)..+3 of word [n/8][kk/32]
+ *   w(n, kk) = (code - zero) * s
+ * Experts are stacked on the outermost axis: W13 = [E][2I][H] (rows [0,I)
+ * gate, [I,2I) up), W2 = [E][H][I].
+ *
+ * Workspace.  gate_up and down_combine need a caller-owned device workspace
+ * of at least moe_workspace_bytes(T, E, k, H, I) bytes.  It must be zero-
+ * filled before its first use (e.g. cudaMemsetAsync or torch.zeros) and is
+ * left zeroed in its control words after every call that completed without
+ * a device error, so it can be reused as is.  Calls that share a workspace
+ * must be ordered on one stream.  It also carries the device error word read
+ * by moe_get_device_error.  After a device error is reported, zero the
+ * workspace again before reusing it.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, k > E, ... */
+    MOE_ERR_UNSUPPORTED = 2,  /* well-formed but outside the supported sizes  */
+    MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required   */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+    MOE_ERR_DEVICE_FLAG = 5   /* a kernel flagged bad data (see below)        */
+} moe_status_t;
+
+/* Bits of the device error word (moe_get_device_error). */
+#define MOE_DEVERR_BAD_EXPERT_ID 0x1u  /* topk_ids entry outside [0, E): pair skipped */
+#define MOE_DEVERR_WAIT_TIMEOUT  0x2u  /* an in-kernel wait gave up; outputs invalid  */
+#define MOE_DEVERR_BAD_METADATA  0x4u  /* offsets / sorted_pair / active list invalid */
+
+/* Version of this ABI (incremented on incompatible change). */
+int moe_abi_version(void);
+
+/* Static English text for a status code (host; never NULL). */
+const char *moe_status_string(int status);
+
+/* Bytes of workspace gate_up and down_combine need for this shape (host,
+ * pure).  Returns 0 for sizes the library rejects. */
+size_t moe_workspace_bytes(int T, int E, int k, int H, int I);
+
+/* Diagnostic: waits for `stream` to finish, copies the device error word of
+ * `workspace` into *flag_out (host), clears it on the device, and returns
+ * MOE_ERR_DEVICE_FLAG if it was nonzero, MOE_OK otherwise.  This is the only
+ * call that synchronises; it is meant for tests and debugging. */
+int moe_get_device_error(void *workspace, size_t ws_bytes, uint32_t *flag_out,
+                         void *stream);
+
+/* Step 1, router.  For each token t: softmax over logits[t][0..E), the k
+ * most probable experts (ties: lower expert index first), and their
+ * probabilities renormalised to sum to one -- equivalently softmax over the
+ * k selected logits.  Selection compares the fp32 logits themselves (softmax
+ * is monotone); -0.0 ranks equal to +0.0; NaN ranks below every number.
+ *   logits   f32 [T][E]   (read)
+ *   topk_ids i32 [T][k]   (written) in rank order
+ *   topk_w   f32 [T][k]   (written)
+ * No workspace. */
+int moe_topk_route(const float *logits, int T, int E, int k,
+                   int32_t *topk_ids, float *topk_w, void *stream);
+
+/* Step 2, active-expert segments.  Groups the P pairs by expert: a stable
+ * counting sort of pair ids by expert id.
+ *   topk_ids       i32 [T][k]  (read) expert of each pair
+ *   expert_offsets i32 [E+1]   (written) segment of expert e is rows
+ *                              [offsets[e], offsets[e+1]); offsets[E] = pairs kept
+ *   sorted_pair    i32 [P]     (written) pair ids, segment after segment,
+ *                              ascending within a segment
+ *   active_experts i32 [E]     (written) experts with a non-empty segment in
+ *                              ascending order, then -1 up to E
+ *   num_active     i32 [1]     (written) number of active experts A
+ * An id outside [0, E) is skipped (its pair is in no segment, trailing
+ * sorted_pair entries are -1) and sets MOE_DEVERR_BAD_EXPERT_ID in the
+ * workspace error word.  workspace may be NULL (then bad ids are skipped
+ * silently); if given it must hold at least 256 bytes. */
+int moe_align_offsets(const int32_t *topk_ids, int T, int E, int k,
+                      int32_t *expert_offsets, int32_t *sorted_pair,
+                      int32_t *active_experts, int32_t *num_active,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/* Step 3, gate/up projection with the int4 dequantisation fused in, and
+ * SiLU(gate) * up.  For every sorted row r of every active expert's segment
+ * (pair p = sorted_pair[r], token t = p / k):
+ *   g_i = sum_K x[t][K] * W13[e][i][K],  u_i = sum_K x[t][K] * W13[e][I+i][K]
+ *   h[r][i] = silu(g_i) * u_i,  silu(v) = v / (1 + exp(-v)),  i in [0, I)
+ *   x     f16 [T][H]                         (read)
+ *   w13_q u32 [E][2I][H/8], w13_s f16 [E][2I][H/32], w13_z u32 [E][2I/8][H/32]
+ *   expert_offsets, sorted_pair, active_experts, num_active: step 2 outputs
+ *   h     f16 [P][I]  (written) in sorted-row order; rows not in any segment
+ *                      are left untouched
+ * Arithmetic: codes minus zero times activation in fp16 within each group of
+ * 32 (exact integer differences, one rounding per product and sum), group
+ * sums scaled and accumulated in fp32, SiLU in fp32, h rounded to fp16.
+ * `h` must not alias any input. */
+int moe_w4a16_gate_up_silu(const uint16_t *x,
+                           const uint32_t *w13_q, const uint16_t *w13_s,
+                           const uint32_t *w13_z, int group_size,
+                           const int32_t *expert_offsets, const int32_t *sorted_pair,
+                           const int32_t *active_experts, const int32_t *num_active,
+                           int T, int E, int k, int H, int I,
+                           uint16_t *h, void *workspace, size_t ws_bytes,
+                           void *stream);
+
+/* Step 4, down projection with the dequantisation fused in, and the
+ * weighted combine.  For every sorted row r (pair p = t*k + j):
+ *   y_p[n] = sum_i h[r][i] * W2[e][n][i],  n in [0, H)
+ *   out[t][n] = sum_{j<k} topk_w[t][j] * y_{t*k+j}[n]   (j in order, fp32)
+ *   h      f16 [P][I]   (read) step 3 output
+ *   w2_q u32 [E][H][I/8], w2_s f16 [E][H][I/32], w2_z u32 [E][H/8][I/32]
+ *   topk_w f32 [T][k]   (read) step 1 weights
+ *   out    f16 [T][H]   (written) rounded from fp32
+ * The per-pair y lives in the workspace in fp32; the combine sums a token's
+ * k terms in a fixed order, so results are deterministic.  `out` may alias
+ * x of step 3 but not h or topk_w. */
+int moe_w4a16_down_combine(const uint16_t *h,
+                           const uint32_t *w2_q, const uint16_t *w2_s,
+                           const uint32_t *w2_z, int group_size,
+                           const int32_t *expert_offsets, const int32_t *sorted_pair,
+                           const int32_t *active_experts, const int32_t *num_active,
+                           const float *topk_w, int T, int E, int k, int H, int I,
+                           uint16_t *out, void *workspace, size_t ws_bytes,
+                           void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4A16_H */

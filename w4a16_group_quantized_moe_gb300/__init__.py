@@ -1,0 +1,271 @@
+"""libmoe_w4a16: the W4A16 group-32 routed-expert MoE layer on GB300.
+
+A thin binding over the C ABI in include/moe_w4a16.h.  The functions below
+have the C names, take PyTorch CUDA tensors (PyTorch only provides device
+memory and streams), and do argument marshalling only: every step of the
+layer runs in the library's CUDA kernels.  There is no fallback path: if the
+native library is missing the calls raise.
+
+Build the library with ``python -m w4a16_group_quantized_moe_gb300.build``
+(or ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_native", "libmoe_w4a16.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_FLAG = 5
+
+MOE_DEVERR_BAD_EXPERT_ID = 0x1
+MOE_DEVERR_WAIT_TIMEOUT = 0x2
+MOE_DEVERR_BAD_METADATA = 0x4
+
+EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes",
+            "moe_get_device_error", "moe_topk_route", "moe_align_offsets",
+            "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine")
+
+_lock = threading.Lock()
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+
+class MoEError(RuntimeError):
+    def __init__(self, call: str, status: int, text: str):
+        super().__init__(f"{call} failed: {text} (status {status})")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libmoe_w4a16.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libmoe_w4a16 native library not found at {path}; build it with "
+                "`python -m w4a16_group_quantized_moe_gb300.build`")
+        lib = ctypes.CDLL(path)
+        lib.moe_abi_version.restype = _I
+        lib.moe_status_string.restype = ctypes.c_char_p
+        lib.moe_status_string.argtypes = [_I]
+        lib.moe_workspace_bytes.restype = _SZ
+        lib.moe_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+        lib.moe_get_device_error.restype = _I
+        lib.moe_get_device_error.argtypes = [_P, _SZ, ctypes.POINTER(ctypes.c_uint32), _P]
+        lib.moe_topk_route.restype = _I
+        lib.moe_topk_route.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+        lib.moe_align_offsets.restype = _I
+        lib.moe_align_offsets.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]
+        lib.moe_w4a16_gate_up_silu.restype = _I
+        lib.moe_w4a16_gate_up_silu.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P,
+                                               _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+        lib.moe_w4a16_down_combine.restype = _I
+        lib.moe_w4a16_down_combine.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
+                                               _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+        _lib = lib
+        return lib
+
+
+def _check(call: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(call, status, load_library().moe_status_string(status).decode())
+
+
+def _dev(t, dtype, name):
+    """Device address of a contiguous CUDA tensor of the given dtype."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def workspace_bytes(T: int, E: int, k: int, H: int, I: int) -> int:
+    return int(load_library().moe_workspace_bytes(T, E, k, H, I))
+
+
+def new_workspace(T: int, E: int, k: int, H: int, I: int, device="cuda"):
+    """A zero-filled workspace of the size the library asks for."""
+    import torch
+    n = workspace_bytes(T, E, k, H, I)
+    if n == 0:
+        raise MoEError("moe_workspace_bytes", MOE_ERR_INVALID_ARG, "sizes rejected")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_get_device_error(workspace, stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device error word."""
+    import torch
+    flag = ctypes.c_uint32(0)
+    st = load_library().moe_get_device_error(_dev(workspace, torch.uint8, "workspace"),
+                                             workspace.numel(), ctypes.byref(flag), _stream(stream))
+    if st not in (MOE_OK, MOE_ERR_DEVICE_FLAG):
+        _check("moe_get_device_error", st)
+    return int(flag.value)
+
+
+def moe_topk_route(logits, k: int, topk_ids=None, topk_w=None, stream=None):
+    import torch
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check("moe_topk_route", load_library().moe_topk_route(
+        _dev(logits, torch.float32, "logits"), T, E, k, _dev(topk_ids, torch.int32, "topk_ids"),
+        _dev(topk_w, torch.float32, "topk_w"), _stream(stream)))
+    return topk_ids, topk_w
+
+
+def moe_align_offsets(topk_ids, E: int, workspace=None, out=None, stream=None):
+    """Returns (expert_offsets[E+1], sorted_pair[P], active_experts[E], num_active[1])."""
+    import torch
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    if out is None:
+        out = (torch.empty(E + 1, dtype=torch.int32, device=dev),
+               torch.empty(T * k, dtype=torch.int32, device=dev),
+               torch.empty(E, dtype=torch.int32, device=dev),
+               torch.empty(1, dtype=torch.int32, device=dev))
+    offs, sp, act, na = out
+    ws = _dev(workspace, torch.uint8, "workspace")
+    _check("moe_align_offsets", load_library().moe_align_offsets(
+        _dev(topk_ids, torch.int32, "topk_ids"), T, E, k, _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), ws, 0 if workspace is None else workspace.numel(),
+        _stream(stream)))
+    return out
+
+
+def moe_w4a16_gate_up_silu(x, w13, meta, k: int, workspace, h=None, stream=None, group_size=32):
+    """h[T*k, I] (fp16, sorted-row order).  w13 = (qweight, scales, qzeros)."""
+    import torch
+    q, s, z = w13
+    T, H = x.shape
+    E, twoI, _ = q.shape
+    I = twoI // 2
+    offs, sp, act, na = meta
+    if h is None:
+        h = torch.empty((T * k, I), dtype=torch.float16, device=x.device)
+    _check("moe_w4a16_gate_up_silu", load_library().moe_w4a16_gate_up_silu(
+        _dev(x, torch.float16, "x"), _dev(q, torch.int32, "w13_q"), _dev(s, torch.float16, "w13_s"),
+        _dev(z, torch.int32, "w13_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), T, E, k, H, I, _dev(h, torch.float16, "h"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return h
+
+
+def moe_w4a16_down_combine(h, w2, meta, topk_w, workspace, out=None, stream=None, group_size=32):
+    """out[T, H] (fp16).  w2 = (qweight, scales, qzeros)."""
+    import torch
+    q, s, z = w2
+    E, H, _ = q.shape
+    T, k = topk_w.shape
+    I = h.shape[1]
+    offs, sp, act, na = meta
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float16, device=h.device)
+    _check("moe_w4a16_down_combine", load_library().moe_w4a16_down_combine(
+        _dev(h, torch.float16, "h"), _dev(q, torch.int32, "w2_q"), _dev(s, torch.float16, "w2_s"),
+        _dev(z, torch.int32, "w2_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), _dev(topk_w, torch.float32, "topk_w"),
+        T, E, k, H, I, _dev(out, torch.float16, "out"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return out
+
+
+def to_device_weights(w, device="cuda"):
+    """(qweight, scales, qzeros) numpy arrays -> CUDA tensors (u32 viewed as int32)."""
+    import numpy as np
+    import torch
+    q, s, z = w
+    return (torch.from_numpy(np.ascontiguousarray(q).view(np.int32)).to(device),
+            torch.from_numpy(np.ascontiguousarray(s)).to(device),
+            torch.from_numpy(np.ascontiguousarray(z).view(np.int32)).to(device))
+
+
+class MoELayer:
+    """Device weights plus preallocated buffers for one (T, E, k, H, I) shape;
+    ``forward`` issues the four calls on one stream."""
+
+    def __init__(self, w13, w2, T: int, k: int, device="cuda"):
+        import torch
+        self.w13, self.w2 = w13, w2
+        E, twoI, H8 = w13[0].shape
+        self.E, self.I, self.H, self.T, self.k = E, twoI // 2, H8 * 8, T, k
+        dev = torch.device(device)
+        P = T * k
+        self.topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.meta = (torch.empty(E + 1, dtype=torch.int32, device=dev),
+                     torch.empty(P, dtype=torch.int32, device=dev),
+                     torch.empty(E, dtype=torch.int32, device=dev),
+                     torch.empty(1, dtype=torch.int32, device=dev))
+        self.h = torch.empty((P, self.I), dtype=torch.float16, device=dev)
+        self.out = torch.empty((T, self.H), dtype=torch.float16, device=dev)
+        self.workspace = new_workspace(T, E, k, self.H, self.I, device=dev)
+
+    def forward(self, logits, x, stream=None):
+        moe_topk_route(logits, self.k, self.topk_ids, self.topk_w, stream=stream)
+        moe_align_offsets(self.topk_ids, self.E, self.workspace, out=self.meta, stream=stream)
+        moe_w4a16_gate_up_silu(x, self.w13, self.meta, self.k, self.workspace, h=self.h,
+                               stream=stream)
+        moe_w4a16_down_combine(self.h, self.w2, self.meta, self.topk_w, self.workspace,
+                               out=self.out, stream=stream)
+        return self.out
+
+    def bind(self, logits, x, stream=None):
+        """Pre-marshals the four calls for fixed input buffers; returns four
+        zero-argument callables (route, align, gate_up, down) that each make
+        one C call.  Used where host overhead must stay off the timeline."""
+        import torch
+        lib = load_library()
+        st = _stream(stream)
+        T, E, k, H, I = self.T, self.E, self.k, self.H, self.I
+        offs, sp, act, na = (t.data_ptr() for t in self.meta)
+        ws, wsb = self.workspace.data_ptr(), self.workspace.numel()
+        _dev(logits, torch.float32, "logits")
+        _dev(x, torch.float16, "x")
+        q13, s13, z13 = (t.data_ptr() for t in self.w13)
+        q2, s2, z2 = (t.data_ptr() for t in self.w2)
+        a_route = (logits.data_ptr(), T, E, k, self.topk_ids.data_ptr(), self.topk_w.data_ptr(), st)
+        a_align = (self.topk_ids.data_ptr(), T, E, k, offs, sp, act, na, ws, wsb, st)
+        a_gu = (x.data_ptr(), q13, s13, z13, 32, offs, sp, act, na, T, E, k, H, I,
+                self.h.data_ptr(), ws, wsb, st)
+        a_dn = (self.h.data_ptr(), q2, s2, z2, 32, offs, sp, act, na, self.topk_w.data_ptr(),
+                T, E, k, H, I, self.out.data_ptr(), ws, wsb, st)
+
+        def call(fn, name, args):
+            def run():
+                status = fn(*args)
+                if status != MOE_OK:
+                    _check(name, status)
+            return run
+        return (call(lib.moe_topk_route, "moe_topk_route", a_route),
+                call(lib.moe_align_offsets, "moe_align_offsets", a_align),
+                call(lib.moe_w4a16_gate_up_silu, "moe_w4a16_gate_up_silu", a_gu),
+                call(lib.moe_w4a16_down_combine, "moe_w4a16_down_combine", a_dn))

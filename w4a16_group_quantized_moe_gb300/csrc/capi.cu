@@ -1,0 +1,207 @@
+// capi.cu -- the extern "C" boundary of libmoe_w4a16 (declared, with the
+// meaning, layout, ownership and error behaviour of every argument, in
+// include/moe_w4a16.h).  Host code only: argument validation, cached device
+// attributes, and kernel dispatch.
+#include <mutex>
+
+#include "common.cuh"
+
+#define MOE_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+cudaError_t launch_route(const float *, int, int, int, int32_t *, float *, cudaStream_t);
+cudaError_t launch_align(const int32_t *, int, int, int32_t *, int32_t *, int32_t *, int32_t *,
+                         uint32_t *, size_t, cudaStream_t);
+cudaError_t launch_gate_up_stream(const __half *, const uint32_t *, const __half *, const uint32_t *,
+                                  const int32_t *, const int32_t *, const int32_t *, const int32_t *,
+                                  int, int, int, int, int, __half *, uint32_t *, int, size_t,
+                                  cudaStream_t);
+cudaError_t launch_down_stream(const __half *, const uint32_t *, const __half *, const uint32_t *,
+                               const int32_t *, const int32_t *, const int32_t *, const int32_t *,
+                               const float *, int, int, int, int, int, __half *, float *, uint32_t *,
+                               uint32_t *, int, size_t, cudaStream_t);
+
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr long long kMaxPairs = 1LL << 24;
+
+struct DeviceInfo {
+    int sms = 0;
+    size_t smem_optin = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_info[128];
+
+// SM count and opt-in shared memory of the current device, queried once.
+cudaError_t device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_info[dev].sms == 0) {
+        int sms = 0, smem = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        g_info[dev].sms = sms;
+        g_info[dev].smem_optin = (size_t)smem;
+    }
+    *out = g_info[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sizes shared by every call.  H or I <= 0 means "not used by this call".
+int check_sizes(int T, int E, int k, int H, int I) {
+    if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (H != -1 && (H <= 0 || H % 32)) return MOE_ERR_INVALID_ARG;
+    if (I != -1 && (I <= 0 || I % 32)) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxE || k > kMaxK || (long long)T * k > kMaxPairs) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int check_group(int group_size) {
+    if (group_size <= 0) return MOE_ERR_INVALID_ARG;
+    return group_size == 32 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+template <typename... Ps>
+bool all_aligned(const Ps *...ps) {
+    bool ok = true;
+    ((ok = ok && ps != nullptr && aligned16(ps)), ...);
+    return ok;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_EXPORT int moe_abi_version(void) { return 1; }
+
+MOE_EXPORT const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size or option";
+        case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_DEVICE_FLAG: return "device kernel flagged invalid data";
+        default: return "unknown status";
+    }
+}
+
+MOE_EXPORT size_t moe_workspace_bytes(int T, int E, int k, int H, int I) {
+    if (check_sizes(T, E, k, H, I) != MOE_OK) return 0;
+    return workspace_layout(T, k, H).total;
+}
+
+MOE_EXPORT int moe_get_device_error(void *workspace, size_t ws_bytes, uint32_t *flag_out,
+                                    void *stream) {
+    if (!workspace || !flag_out || ws_bytes < kCtrlBytes || !aligned16(workspace))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && v) {
+        e = cudaMemsetAsync(workspace, 0, sizeof(v), s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *flag_out = v;
+    return v ? MOE_ERR_DEVICE_FLAG : MOE_OK;
+}
+
+MOE_EXPORT int moe_topk_route(const float *logits, int T, int E, int k, int32_t *topk_ids,
+                              float *topk_w, void *stream) {
+    int st = check_sizes(T, E, k, -1, -1);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(logits, topk_ids, topk_w)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    return cuda_status(launch_route(logits, T, E, k, topk_ids, topk_w, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_align_offsets(const int32_t *topk_ids, int T, int E, int k,
+                                 int32_t *expert_offsets, int32_t *sorted_pair,
+                                 int32_t *active_experts, int32_t *num_active, void *workspace,
+                                 size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, -1, -1);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(topk_ids, expert_offsets, sorted_pair, active_experts, num_active))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace && (ws_bytes < kCtrlBytes || !aligned16(workspace))) return MOE_ERR_WORKSPACE;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    // T == 0 still defines the outputs: empty segments, no active experts
+    return cuda_status(launch_align(topk_ids, T * k, E, expert_offsets, sorted_pair, active_experts,
+                                    num_active, static_cast<uint32_t *>(workspace), di.smem_optin,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
+                                      const uint16_t *w13_s, const uint32_t *w13_z, int group_size,
+                                      const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                      const int32_t *active_experts, const int32_t *num_active,
+                                      int T, int E, int k, int H, int I, uint16_t *h,
+                                      void *workspace, size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if ((st = check_group(group_size)) != MOE_OK) return st;
+    if (!all_aligned(x, w13_q, w13_s, w13_z, expert_offsets, sorted_pair, active_experts,
+                     num_active, h))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t *err = static_cast<uint32_t *>(workspace) + kCtrlErrorWord;
+    e = launch_gate_up_stream(reinterpret_cast<const __half *>(x), w13_q,
+                              reinterpret_cast<const __half *>(w13_s), w13_z, expert_offsets,
+                              sorted_pair, active_experts, num_active, T, E, k, H, I,
+                              reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin,
+                              static_cast<cudaStream_t>(stream));
+    return cuda_status(e);
+}
+
+MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
+                                      const uint32_t *w2_z, int group_size,
+                                      const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                      const int32_t *active_experts, const int32_t *num_active,
+                                      const float *topk_w, int T, int E, int k, int H, int I,
+                                      uint16_t *out, void *workspace, size_t ws_bytes,
+                                      void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if ((st = check_group(group_size)) != MOE_OK) return st;
+    if (!all_aligned(h, w2_q, w2_s, w2_z, expert_offsets, sorted_pair, active_experts, num_active,
+                     topk_w, out))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const WorkspaceLayout L = workspace_layout(T, k, H);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
+    e = launch_down_stream(reinterpret_cast<const __half *>(h), w2_q,
+                           reinterpret_cast<const __half *>(w2_s), w2_z, expert_offsets, sorted_pair,
+                           active_experts, num_active, topk_w, T, E, k, H, I,
+                           reinterpret_cast<__half *>(out), reinterpret_cast<float *>(ws + L.y),
+                           reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms,
+                           di.smem_optin, static_cast<cudaStream_t>(stream));
+    return cuda_status(e);
+}

@@ -1,0 +1,158 @@
+// common.cuh -- device helpers shared by the libmoe_w4a16 kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_w4a16.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- workspace
+// Control block at the start of the workspace.
+constexpr size_t kCtrlBytes = 256;
+constexpr int kCtrlErrorWord = 0;     // u32: MOE_DEVERR_* bits
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace regions after the control block (all 256-byte aligned).
+struct WorkspaceLayout {
+    size_t counters;   // u32 [H/8]: arrivals per 8-row output block (down, decode)
+    size_t y;          // f32 [P][H]: per-pair down projection
+    size_t total;
+};
+
+__host__ __device__ inline WorkspaceLayout workspace_layout(int T, int k, int H) {
+    WorkspaceLayout L;
+    L.counters = kCtrlBytes;
+    L.y = L.counters + align_up((size_t)(H / 8) * 4, 256);
+    L.total = L.y + align_up((size_t)T * k * H * 4, 256);
+    return L;
+}
+
+__device__ inline void set_error(uint32_t *err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ inline uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ inline void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ inline void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ inline void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a barrier phase.  Gives up after roughly a second (far
+// beyond any legitimate wait here) and returns false so the caller can flag
+// the error and leave instead of hanging the GPU.  `abort_flag` (shared)
+// lets one thread's failure release every other waiter of the CTA.
+constexpr uint32_t kWaitSpins = 1u << 22;
+
+__device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                         volatile int *abort_flag) {
+    for (uint32_t it = 0; it < kWaitSpins; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (it > 256) __nanosleep(128);
+    }
+    return false;
+}
+
+// One bulk copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Named barrier for a subset of the CTA's warps (id 0 is __syncthreads).
+__device__ inline void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- int4 dequant
+// Codes of one 32-bit word (8 codes, code j in bits 4j..4j+3) minus the zero
+// point, as four fp16 pairs, straight from the binary16 format: 0x6400 is
+// 1024.0 and binary16 values in [1024, 2048) are spaced exactly 1 apart, so
+// OR-ing a 4-bit field into the low mantissa bits gives exactly 1024 + code,
+// and a field sitting at bits 4..7 gives exactly 1024 + 16*code.  Subtracting
+// (1024 + z), or scaling by 1/16 and subtracting (64 + z) in one fused
+// multiply-add, leaves code - z exactly (a small integer).  Two codes per
+// instruction, with no integer-to-float conversion.
+//
+// Output pairing: d[0] = (c0, c4), d[1] = (c1, c5), d[2] = (c2, c6),
+// d[3] = (c3, c7) (low half first).  Activations are staged in the matching
+// order [a0 a4 a1 a5 a2 a6 a3 a7] per block of eight.
+struct ZeroPoint {
+    __half2 z1024;    // (1024 + z, 1024 + z)
+    __half2 neg_z64;  // (-(64 + z), -(64 + z))
+};
+
+__device__ inline ZeroPoint make_zero_point(uint32_t z) {
+    ZeroPoint zp;
+    uint32_t bits = (0x6400u | z) * 0x00010001u;
+    zp.z1024 = *reinterpret_cast<__half2 *>(&bits);
+    zp.neg_z64 = __hsub2(__float2half2_rn(960.0f), zp.z1024);
+    return zp;
+}
+
+__device__ inline void dequant_word(uint32_t w, const ZeroPoint &zp, __half2 *d) {
+    const uint32_t lo = (w & 0x000F000Fu) | 0x64006400u;
+    const uint32_t hi = (w & 0x00F000F0u) | 0x64006400u;
+    const uint32_t w8 = w >> 8;
+    const uint32_t lo2 = (w8 & 0x000F000Fu) | 0x64006400u;
+    const uint32_t hi2 = (w8 & 0x00F000F0u) | 0x64006400u;
+    const __half2 sixteenth = __float2half2_rn(0.0625f);
+    d[0] = __hsub2(*reinterpret_cast<const __half2 *>(&lo), zp.z1024);
+    d[1] = __hfma2(*reinterpret_cast<const __half2 *>(&hi), sixteenth, zp.neg_z64);
+    d[2] = __hsub2(*reinterpret_cast<const __half2 *>(&lo2), zp.z1024);
+    d[3] = __hfma2(*reinterpret_cast<const __half2 *>(&hi2), sixteenth, zp.neg_z64);
+}
+
+// Reorders eight fp16 values [a0..a7] (one uint4) into the pairing used by
+// dequant_word: [a0 a4 a1 a5 a2 a6 a3 a7].
+__device__ inline uint4 pair_interleave(uint4 v) {
+    uint4 o;
+    o.x = __byte_perm(v.x, v.z, 0x5410);
+    o.y = __byte_perm(v.x, v.z, 0x7632);
+    o.z = __byte_perm(v.y, v.w, 0x5410);
+    o.w = __byte_perm(v.y, v.w, 0x7632);
+    return o;
+}
+
+__device__ inline __half2 u32_as_half2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
+
+}  // namespace moe
