@@ -6,7 +6,9 @@ HBM.  Default workload: Qwen4Exp-geometry decode, 1 token (hidden 2560,
 intermediate 640, 512 experts, top-10, W4A16 g32).
 
 Timing: W untimed warm-up steps, then K timed steps.  Before every step L2
-is flushed by writing a 1 GiB buffer (outside the timed interval) and the
+is flushed by reading a 1 GiB buffer (outside the timed interval; a read
+leaves clean lines behind, so the step does not pay for write-backs of the
+flush itself) and the
 router logits rotate over 32 pre-generated sets so the active experts change
 from step to step.  Each step is bracketed by CUDA events on the launching
 stream, with events around the gate/up kernel for the roofline line.  The
@@ -237,7 +239,11 @@ def main():
     x_buf = torch.empty((T, H), dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
     route, align, gate_up, down = layer.bind(logits_buf, x_buf, stream)
-    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones((args.flush_mb << 20) // 4, dtype=torch.int32, device=dev)
+    flush_out = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        torch.sum(flush, dim=0, dtype=torch.int64, out=flush_out)
 
     # active-expert count of every logits set (for the algorithmic bytes)
     A_of = []
@@ -251,7 +257,7 @@ def main():
         lg, xx = sets[s % len(sets)]
         logits_buf.copy_(lg, non_blocking=True)
         x_buf.copy_(xx, non_blocking=True)
-        flush.fill_(s & 0xFF)
+        flush_l2()
         if ev is not None:
             ev[0].record(stream)
         route(); align()
@@ -308,7 +314,7 @@ def main():
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
     for s in range(e2e_steps):
         i = s % len(sets)
-        flush.fill_(s & 0xFF)
+        flush_l2()
         e2e_ev[s][0].record(stream)
         logits_buf.copy_(h_logits[i], non_blocking=True)
         x_buf.copy_(h_x[i], non_blocking=True)
@@ -338,7 +344,7 @@ def main():
             "dtype": "f16", "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
                        "group_size": 32, "parallelism": f"replicas x{world}",
-                       "l2": f"flushed before every timed step ({args.flush_mb} MiB write); "
+                       "l2": f"flushed before every timed step ({args.flush_mb} MiB read); "
                              f"router logits rotated over {args.sets} sets",
                        "mean_active_experts": float(A_steps.mean())},
             "layer_hbm_gbs": layer_gbs,

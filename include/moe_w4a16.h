@@ -29,8 +29,8 @@
  *   - T = tokens, E = experts, k = experts per token, H = hidden size,
  *     I = expert intermediate size, P = T*k token-expert pairs.  A pair is
  *     p = t*k + j: token t's j-th selected expert.
- *   - Supported sizes: 0 <= T, 1 <= k <= min(E, 32), E <= 1024,
- *     H and I positive multiples of 32, group_size == 32.  Anything else is
+ *   - Supported sizes: 0 <= T, T*k <= 2^24, 1 <= k <= min(E, 32), E <= 1024,
+ *     H and I positive multiples of 32 up to 65536, group_size == 32.  Anything else is
  *     MOE_ERR_INVALID_ARG (malformed) or MOE_ERR_UNSUPPORTED (outside the
  *     sizes above).  T == 0 is a no-op that returns MOE_OK.
  *
@@ -119,7 +119,8 @@ int moe_topk_route(const float *logits, int T, int E, int k,
  * An id outside [0, E) is skipped (its pair is in no segment, trailing
  * sorted_pair entries are -1) and sets MOE_DEVERR_BAD_EXPERT_ID in the
  * workspace error word.  workspace may be NULL (then bad ids are skipped
- * silently); if given it must hold at least 256 bytes. */
+ * silently); if given it must hold at least 256 bytes.  With T == 0,
+ * topk_ids and sorted_pair may be NULL. */
 int moe_align_offsets(const int32_t *topk_ids, int T, int E, int k,
                       int32_t *expert_offsets, int32_t *sorted_pair,
                       int32_t *active_experts, int32_t *num_active,

@@ -92,6 +92,8 @@ __global__ void align_kernel(const int32_t *__restrict__ topk_ids, int P, int E,
     int *scratch = slot + E;        // [128]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    pdl_wait();
+    pdl_trigger();
     for (int i = tid; i < W * E; i += blockDim.x) hist[i] = 0;
     __syncthreads();
 
@@ -168,14 +170,11 @@ cudaError_t launch_align(const int32_t *ids, int P, int E, int32_t *offsets, int
                          cudaStream_t stream) {
     const int W = align_warps(P, E, smem_limit);
     const size_t smem = align_smem_bytes(W, E);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    align_kernel<<<1, W * 32, smem, stream>>>(ids, P, E, offsets, sorted_pair, active, num_active,
-                                              err);
-    return cudaGetLastError();
+    static int configured[128];
+    cudaError_t e = ensure_smem(align_kernel, configured, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(align_kernel, 1, W * 32, smem, stream, ids, P, E, offsets, sorted_pair, active,
+                      num_active, err);
 }
 
 }  // namespace moe

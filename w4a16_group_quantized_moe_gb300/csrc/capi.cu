@@ -26,6 +26,7 @@ namespace {
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
 constexpr long long kMaxPairs = 1LL << 24;
+constexpr int kMaxDim = 1 << 16;
 
 struct DeviceInfo {
     int sms = 0;
@@ -63,6 +64,7 @@ int check_sizes(int T, int E, int k, int H, int I) {
     if (H != -1 && (H <= 0 || H % 32)) return MOE_ERR_INVALID_ARG;
     if (I != -1 && (I <= 0 || I % 32)) return MOE_ERR_INVALID_ARG;
     if (E > kMaxE || k > kMaxK || (long long)T * k > kMaxPairs) return MOE_ERR_UNSUPPORTED;
+    if (H > kMaxDim || I > kMaxDim) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -136,8 +138,9 @@ MOE_EXPORT int moe_align_offsets(const int32_t *topk_ids, int T, int E, int k,
                                  size_t ws_bytes, void *stream) {
     int st = check_sizes(T, E, k, -1, -1);
     if (st != MOE_OK) return st;
-    if (!all_aligned(topk_ids, expert_offsets, sorted_pair, active_experts, num_active))
-        return MOE_ERR_INVALID_ARG;
+    if (!all_aligned(expert_offsets, active_experts, num_active)) return MOE_ERR_INVALID_ARG;
+    // with no pairs the id and pair buffers are empty and may be NULL
+    if (T > 0 && !all_aligned(topk_ids, sorted_pair)) return MOE_ERR_INVALID_ARG;
     if (workspace && (ws_bytes < kCtrlBytes || !aligned16(workspace))) return MOE_ERR_WORKSPACE;
     DeviceInfo di;
     cudaError_t e = device_info(&di);

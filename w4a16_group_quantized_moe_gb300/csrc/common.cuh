@@ -60,30 +60,33 @@ __device__ inline void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Waits (suspended, not spinning) for the phase of `parity` to complete, for
+// at most about kSuspendHintNs; returns whether it completed.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
 
-// Bounded wait on a barrier phase.  Gives up after roughly a second (far
+// Bounded wait on a barrier phase.  Gives up after about a second (far
 // beyond any legitimate wait here) and returns false so the caller can flag
 // the error and leave instead of hanging the GPU.  `abort_flag` (shared)
 // lets one thread's failure release every other waiter of the CTA.
-constexpr uint32_t kWaitSpins = 1u << 22;
+constexpr uint32_t kWaitTries = 1024;
 
 __device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                          volatile int *abort_flag) {
-    for (uint32_t it = 0; it < kWaitSpins; ++it) {
+    for (uint32_t it = 0; it < kWaitTries; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort_flag && *abort_flag) return false;
-        if (it > 256) __nanosleep(128);
     }
     return false;
 }
@@ -98,9 +101,60 @@ __device__ inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint
         : "memory");
 }
 
+// 16-byte read of data used once (packed weights): read-only path, not kept
+// in L1.
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
 // Named barrier for a subset of the CTA's warps (id 0 is __syncthreads).
 __device__ inline void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: every kernel of the library is launched
+// with programmatic stream serialisation, so it can be scheduled while its
+// predecessor on the stream is still running.  Protocol, for every kernel:
+// nothing before pdl_wait() reads global memory (only barrier set-up runs
+// there); pdl_wait() returns once the predecessor grid has completed and its
+// writes are visible; pdl_trigger() right after lets the successor start its
+// own set-up.  So every kernel still sees all earlier work on the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device and size.
+template <typename K>
+inline cudaError_t ensure_smem(K kernel, int *configured /* [128] */, size_t smem) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (configured[dev] >= (int)smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) configured[dev] = (int)smem;
+    return e;
 }
 
 // ---------------------------------------------------------------- int4 dequant

@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
         *abort_flag = 0;
         fence_mbar_init();
     }
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
 
     int A = __ldg(a.num_active);
@@ -402,6 +404,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const StreamA
 // out[t][n] = sum_j topk_w[t][j] * y[t*k+j][n], j in order; 8 outputs/thread.
 __global__ void combine_kernel(const float *__restrict__ y, const float *__restrict__ topk_w, int T,
                                int k, int H, __half *__restrict__ out) {
+    pdl_wait();
+    pdl_trigger();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const int HB = H / 8;
     if (idx >= (long long)T * HB) return;
@@ -444,14 +448,13 @@ static cudaError_t launch_stream_t(StreamArgs a, int num_sms, size_t smem_limit,
     nst = nst > kMaxStages ? kMaxStages : nst;
     a.nstages = nst;
     const size_t smem = fixed + (size_t)nst * geom.bytes;
-    cudaError_t e = cudaFuncSetAttribute(stream_kernel<MODE, S>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int configured[128];
+    cudaError_t e = ensure_smem(stream_kernel<MODE, S>, configured, smem);
     if (e != cudaSuccess) return e;
     const long long amax = a.E < a.P ? a.E : a.P;
     const long long units = (amax * a.rows + RS - 1) / RS;
     const int grid = (int)(units < num_sms ? (units < 1 ? 1 : units) : num_sms);
-    stream_kernel<MODE, S><<<grid, kStreamThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(stream_kernel<MODE, S>, grid, kStreamThreads, smem, stream, a);
 }
 
 cudaError_t launch_gate_up_stream(const __half *x, const uint32_t *q, const __half *s,
@@ -491,8 +494,8 @@ cudaError_t launch_down_stream(const __half *h, const uint32_t *q, const __half 
         e = launch_stream_t<kDown, 4>(a, num_sms, smem_limit, stream);
     if (e != cudaSuccess || a.fuse_combine) return e;
     const long long n = (long long)T * (H / 8);
-    combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(y, topk_w, T, k, H, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, (unsigned)((n + 255) / 256), 256, 0, stream,
+                      (const float *)y, topk_w, T, k, H, out);
 }
 
 }  // namespace moe
