@@ -21,6 +21,16 @@ cudaError_t launch_down_stream(const __half *, const uint32_t *, const __half *,
                                const float *, int, int, int, int, int, __half *, float *, uint32_t *,
                                uint32_t *, int, size_t, cudaStream_t);
 
+bool decode_supported(int, int, int, int, int, size_t);
+cudaError_t launch_gate_up_decode(const __half *, const uint32_t *, const __half *, const uint32_t *,
+                                  const int32_t *, const int32_t *, const int32_t *, const int32_t *,
+                                  int, int, int, int, int, __half *, uint32_t *, int, size_t,
+                                  cudaStream_t);
+cudaError_t launch_down_decode(const __half *, const uint32_t *, const __half *, const uint32_t *,
+                               const int32_t *, const int32_t *, const int32_t *, const int32_t *,
+                               const float *, int, int, int, int, int, __half *, float *, uint32_t *,
+                               uint32_t *, int, size_t, cudaStream_t);
+
 namespace {
 
 constexpr int kMaxE = 1024;
@@ -170,6 +180,12 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     uint32_t *err = static_cast<uint32_t *>(workspace) + kCtrlErrorWord;
+    // dispatch by shape only: decode batches take the latency-first kernel
+    if (decode_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_gate_up_decode(
+            reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,
+            expert_offsets, sorted_pair, active_experts, num_active, T, E, k, H, I,
+            reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
     e = launch_gate_up_stream(reinterpret_cast<const __half *>(x), w13_q,
                               reinterpret_cast<const __half *>(w13_s), w13_z, expert_offsets,
                               sorted_pair, active_experts, num_active, T, E, k, H, I,
@@ -200,6 +216,13 @@ MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, c
     const WorkspaceLayout L = workspace_layout(T, k, H);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
+    if (decode_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_down_decode(
+            reinterpret_cast<const __half *>(h), w2_q, reinterpret_cast<const __half *>(w2_s), w2_z,
+            expert_offsets, sorted_pair, active_experts, num_active, topk_w, T, E, k, H, I,
+            reinterpret_cast<__half *>(out), reinterpret_cast<float *>(ws + L.y),
+            reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms, di.smem_optin,
+            static_cast<cudaStream_t>(stream)));
     e = launch_down_stream(reinterpret_cast<const __half *>(h), w2_q,
                            reinterpret_cast<const __half *>(w2_s), w2_z, expert_offsets, sorted_pair,
                            active_experts, num_active, topk_w, T, E, k, H, I,
