@@ -169,6 +169,42 @@ int moe_w4a16_down_combine(const uint16_t *h,
                            uint16_t *out, void *workspace, size_t ws_bytes,
                            void *stream);
 
+/* Step 4 for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this is a convenience of this library.  Some callers are not
+ * allowed to call cudaMalloc -- an engine that plans all device memory
+ * before serving and forbids allocation afterwards, a plugin inside a host
+ * application that owns the allocators, a latency-critical loop where an
+ * allocation could synchronise the device -- so they cannot provide the
+ * workspace moe_w4a16_down_combine needs.
+ *
+ * Same arguments, meaning and results as moe_w4a16_down_combine, without
+ * the workspace.  Instead the library keeps one scratch array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes in device memory, which every GPU that
+ * loads the library holds until the process exits.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Shapes whose moe_workspace_bytes(T, E, k, H, I) exceeds
+ *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_UNSUPPORTED before
+ *     anything is launched (at k = 10, H = 2560 that allows T <= 81).  Other
+ *     size errors are those of moe_w4a16_down_combine.
+ *   - The first call on a device looks up the scratch array's device
+ *     address (with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     each call clears the parts that must start at zero (an asynchronous
+ *     memset on `stream`).  Calls that overlap on the GPU, on any stream,
+ *     race on the array and give wrong results: order them.
+ *   - Device-detected errors are written to the scratch's error word, which
+ *     moe_get_device_error cannot reach; the next call clears it. */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+int moe_w4a16_down_combine_noalloc(const uint16_t *h,
+                                   const uint32_t *w2_q, const uint16_t *w2_s,
+                                   const uint32_t *w2_z, int group_size,
+                                   const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                   const int32_t *active_experts, const int32_t *num_active,
+                                   const float *topk_w, int T, int E, int k, int H, int I,
+                                   uint16_t *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

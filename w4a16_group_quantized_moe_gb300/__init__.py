@@ -31,7 +31,8 @@ MOE_DEVERR_BAD_METADATA = 0x4
 
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes",
             "moe_get_device_error", "moe_topk_route", "moe_align_offsets",
-            "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine")
+            "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine",
+            "moe_w4a16_down_combine_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +75,9 @@ def load_library(path: str = LIB_PATH):
         lib.moe_w4a16_down_combine.restype = _I
         lib.moe_w4a16_down_combine.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+        lib.moe_w4a16_down_combine_noalloc.restype = _I
+        lib.moe_w4a16_down_combine_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
+                                                       _I, _I, _I, _I, _I, _P, _P]
         _lib = lib
         return lib
 
@@ -195,6 +199,27 @@ def moe_w4a16_down_combine(h, w2, meta, topk_w, workspace, out=None, stream=None
         _dev(na, torch.int32, "num_active"), _dev(topk_w, torch.float32, "topk_w"),
         T, E, k, H, I, _dev(out, torch.float16, "out"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return out
+
+
+def moe_w4a16_down_combine_noalloc(h, w2, meta, topk_w, out=None, stream=None, group_size=32):
+    """out[T, H] (fp16) like moe_w4a16_down_combine, for callers that cannot
+    allocate a workspace: the library's own fixed scratch array is used
+    instead (see include/moe_w4a16.h; calls that overlap on the GPU race)."""
+    import torch
+    q, s, z = w2
+    E, H, _ = q.shape
+    T, k = topk_w.shape
+    I = h.shape[1]
+    offs, sp, act, na = meta
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float16, device=h.device)
+    _check("moe_w4a16_down_combine_noalloc", load_library().moe_w4a16_down_combine_noalloc(
+        _dev(h, torch.float16, "h"), _dev(q, torch.int32, "w2_q"), _dev(s, torch.float16, "w2_s"),
+        _dev(z, torch.int32, "w2_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), _dev(topk_w, torch.float32, "topk_w"),
+        T, E, k, H, I, _dev(out, torch.float16, "out"), _stream(stream)))
     return out
 
 
