@@ -126,6 +126,19 @@ int moe_align_offsets(const int32_t *topk_ids, int T, int E, int k,
                       int32_t *active_experts, int32_t *num_active,
                       void *workspace, size_t ws_bytes, void *stream);
 
+/* Steps 1 and 2 together: exactly the outputs of moe_topk_route followed by
+ * moe_align_offsets on the same arguments (same layouts, error bits and
+ * workspace rules).  For T <= 32 both steps run in one launch (one CTA),
+ * which removes a kernel launch and a global-memory round trip from the
+ * decode critical path; larger batches run the two kernels.  Reference: the
+ * grouped-decode route of "[Perf][SM70] Narrow Qwen3.8 AWQ active grouped
+ * decode" (section Purpose) prepares routing and segments for 2-8 tokens. */
+int moe_topk_route_align(const float *logits, int T, int E, int k,
+                         int32_t *topk_ids, float *topk_w,
+                         int32_t *expert_offsets, int32_t *sorted_pair,
+                         int32_t *active_experts, int32_t *num_active,
+                         void *workspace, size_t ws_bytes, void *stream);
+
 /* Step 3, gate/up projection with the int4 dequantisation fused in, and
  * SiLU(gate) * up.  For every sorted row r of every active expert's segment
  * (pair p = sorted_pair[r], token t = p / k):

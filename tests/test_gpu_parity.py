@@ -240,3 +240,49 @@ def test_rejects_bad_arguments_without_launching(moe):
     lib = moe.load_library()
     assert lib.moe_topk_route(x.data_ptr() + 4, 2, 64, 4, x.data_ptr(), x.data_ptr(),
                               None) == moe.MOE_ERR_INVALID_ARG   # misaligned
+
+
+@pytest.mark.parametrize("T,E,k,hot", [(1, 512, 10, False), (8, 512, 10, False), (8, 512, 10, True),
+                                       (32, 64, 6, False), (33, 64, 6, False), (4, 16, 2, False),
+                                       (5, 7, 7, False), (2, 1024, 32, False)])
+def test_route_align_fused_matches_oracle(moe, T, E, k, hot):
+    """Steps 1-2 in one call (one launch for T <= 32, two kernels above)."""
+    logits = inputs.make_activations(T, 32, E, seed=T * 3 + E, hot_experts=range(16) if hot else (),
+                                     hot_bias=2.0)[0]
+    if T > 1:
+        logits[1, 2] = logits[1, min(5, E - 1)] = 7.5   # planted tie at the top
+    ids, w, meta = moe.moe_topk_route_align(torch.from_numpy(logits).cuda(), k)
+    ref_ids, ref_w = oracle.route(logits, k)
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=0, atol=1e-6)
+    r_offs, r_sp, r_act, r_na = oracle.align(ref_ids, E)
+    offs, sp, act, na = (t.cpu().numpy() for t in meta)
+    assert np.array_equal(offs, r_offs) and np.array_equal(sp, r_sp)
+    assert np.array_equal(act, r_act) and int(na[0]) == r_na
+
+
+@pytest.mark.parametrize("T", [1, 3, 12])
+def test_duplicate_experts_within_a_token(moe, T):
+    """Caller-supplied ids may repeat an expert inside a token: segments then
+    hold more rows than tokens.  Steps 2-4 against the oracle on the same ids
+    and weights."""
+    E, k, H, I = 16, 6, 256, 64
+    rng = np.random.default_rng(T)
+    ids = rng.integers(0, 4, size=(T, k)).astype(np.int32)      # heavy repeats
+    ids[0, :] = 2                                               # one expert k times
+    tw = rng.random((T, k)).astype(np.float32)
+    x = inputs.make_activations(T, H, E, seed=T)[1]
+    w13, w2, dw13, dw2 = weights(E, H, I, 0)
+    ws = moe.new_workspace(T, E, k, H, I)
+    meta = moe.moe_align_offsets(torch.from_numpy(ids).cuda(), E, workspace=ws)
+    h = moe.moe_w4a16_gate_up_silu(torch.from_numpy(x).cuda(), dw13, meta, k, ws)
+    out = moe.moe_w4a16_down_combine(h, dw2, meta, torch.from_numpy(tw).cuda(), ws)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_error(ws) == 0
+    rmeta = oracle.align(ids, E)
+    for got, ref in zip(meta, rmeta[:3]):
+        assert np.array_equal(got.cpu().numpy(), ref)
+    rh = oracle.gate_up_silu(x, w13, rmeta, k)
+    assert_close(h.float().cpu().numpy(), rh, "dup h")
+    rout = oracle.down_combine(rh, w2, rmeta, tw.astype(np.float64), T, k)
+    assert_close(out.float().cpu().numpy(), rout, "dup out")

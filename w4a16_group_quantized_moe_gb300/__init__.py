@@ -30,7 +30,7 @@ MOE_DEVERR_WAIT_TIMEOUT = 0x2
 MOE_DEVERR_BAD_METADATA = 0x4
 
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes",
-            "moe_get_device_error", "moe_topk_route", "moe_align_offsets",
+            "moe_get_device_error", "moe_topk_route", "moe_align_offsets", "moe_topk_route_align",
             "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine",
             "moe_w4a16_down_combine_noalloc")
 
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_topk_route.argtypes = [_P, _I, _I, _I, _P, _P, _P]
         lib.moe_align_offsets.restype = _I
         lib.moe_align_offsets.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]
+        lib.moe_topk_route_align.restype = _I
+        lib.moe_topk_route_align.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
         lib.moe_w4a16_gate_up_silu.restype = _I
         lib.moe_w4a16_gate_up_silu.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P,
                                                _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
@@ -161,6 +163,31 @@ def moe_align_offsets(topk_ids, E: int, workspace=None, out=None, stream=None):
         _dev(na, torch.int32, "num_active"), ws, 0 if workspace is None else workspace.numel(),
         _stream(stream)))
     return out
+
+
+def moe_topk_route_align(logits, k: int, workspace=None, topk_ids=None, topk_w=None, meta=None,
+                         stream=None):
+    """Steps 1 and 2 in one call: (topk_ids, topk_w, meta)."""
+    import torch
+    T, E = logits.shape
+    dev = logits.device
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if meta is None:
+        meta = (torch.empty(E + 1, dtype=torch.int32, device=dev),
+                torch.empty(T * k, dtype=torch.int32, device=dev),
+                torch.empty(E, dtype=torch.int32, device=dev),
+                torch.empty(1, dtype=torch.int32, device=dev))
+    offs, sp, act, na = meta
+    _check("moe_topk_route_align", load_library().moe_topk_route_align(
+        _dev(logits, torch.float32, "logits"), T, E, k, _dev(topk_ids, torch.int32, "topk_ids"),
+        _dev(topk_w, torch.float32, "topk_w"), _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), _dev(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
+    return topk_ids, topk_w, meta
 
 
 def moe_w4a16_gate_up_silu(x, w13, meta, k: int, workspace, h=None, stream=None, group_size=32):
@@ -266,7 +293,8 @@ class MoELayer:
     def bind(self, logits, x, stream=None):
         """Pre-marshals the four calls for fixed input buffers; returns four
         zero-argument callables (route, align, gate_up, down) that each make
-        one C call.  Used where host overhead must stay off the timeline."""
+        one C call, and sets self.route_align_call (steps 1-2 in one call).
+        Used where host overhead must stay off the timeline."""
         import torch
         lib = load_library()
         st = _stream(stream)
@@ -290,6 +318,9 @@ class MoELayer:
                 if status != MOE_OK:
                     _check(name, status)
             return run
+        a_ra = (logits.data_ptr(), T, E, k, self.topk_ids.data_ptr(), self.topk_w.data_ptr(),
+                offs, sp, act, na, ws, wsb, st)
+        self.route_align_call = call(lib.moe_topk_route_align, "moe_topk_route_align", a_ra)
         return (call(lib.moe_topk_route, "moe_topk_route", a_route),
                 call(lib.moe_align_offsets, "moe_align_offsets", a_align),
                 call(lib.moe_w4a16_gate_up_silu, "moe_w4a16_gate_up_silu", a_gu),

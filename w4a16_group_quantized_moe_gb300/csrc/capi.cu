@@ -22,6 +22,9 @@ cudaError_t launch_down_stream(const __half *, const uint32_t *, const __half *,
                                uint32_t *, int, size_t, cudaStream_t);
 
 bool decode_supported(int, int, int, int, int, size_t);
+bool route_align_fusable(int, int, int, size_t);
+cudaError_t launch_route_align(const float *, int, int, int, int32_t *, float *, int32_t *, int32_t *,
+                               int32_t *, int32_t *, uint32_t *, cudaStream_t);
 cudaError_t launch_gate_up_decode(const __half *, const uint32_t *, const __half *, const uint32_t *,
                                   const int32_t *, const int32_t *, const int32_t *, const int32_t *,
                                   int, int, int, int, int, __half *, uint32_t *, int, size_t,
@@ -159,6 +162,31 @@ MOE_EXPORT int moe_align_offsets(const int32_t *topk_ids, int T, int E, int k,
     return cuda_status(launch_align(topk_ids, T * k, E, expert_offsets, sorted_pair, active_experts,
                                     num_active, static_cast<uint32_t *>(workspace), di.smem_optin,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_topk_route_align(const float *logits, int T, int E, int k, int32_t *topk_ids,
+                                    float *topk_w, int32_t *expert_offsets, int32_t *sorted_pair,
+                                    int32_t *active_experts, int32_t *num_active, void *workspace,
+                                    size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, -1, -1);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(expert_offsets, active_experts, num_active)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !all_aligned(logits, topk_ids, topk_w, sorted_pair)) return MOE_ERR_INVALID_ARG;
+    if (workspace && (ws_bytes < kCtrlBytes || !aligned16(workspace))) return MOE_ERR_WORKSPACE;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t *err = static_cast<uint32_t *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > 0 && route_align_fusable(T, E, k, di.smem_optin))
+        return cuda_status(launch_route_align(logits, T, E, k, topk_ids, topk_w, expert_offsets,
+                                              sorted_pair, active_experts, num_active, err, s));
+    if (T > 0) {
+        e = launch_route(logits, T, E, k, topk_ids, topk_w, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return cuda_status(launch_align(topk_ids, T * k, E, expert_offsets, sorted_pair, active_experts,
+                                    num_active, err, di.smem_optin, s));
 }
 
 MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,

@@ -91,6 +91,12 @@ __device__ inline bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
     return false;
 }
 
+// Orders this thread's earlier generic-proxy accesses to shared memory
+// before its later async-proxy (bulk copy) accesses.
+__device__ inline void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // One bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ inline void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

@@ -7,7 +7,7 @@
 // matters is how soon every SM has its share in flight and how many
 // independent instructions each warp can issue:
 //
-//  * One 16-warp CTA per SM.  A prologue, run by every thread with all loads
+//  * One 14-warp CTA per SM.  A prologue, run by every thread with all loads
 //    issued before any store, brings the routing metadata (active list,
 //    offsets, pair ids) and, in step 3, every x row into shared memory in a
 //    single round trip.  Step 4 caches the h rows of the CTA's segments (one
@@ -15,12 +15,14 @@
 //  * Work is cut into warp tasks: RT consecutive row units (gate/up row pairs
 //    in step 3, output rows in step 4) of one active expert, L lanes per row
 //    unit.  Task lists are split into equal contiguous ranges per warp.
-//  * A warp walks its tasks in steps of kGPI groups per row: the loads of a
-//    step (16-byte code words plus the matching scale and zero words) go
-//    straight into registers one step ahead, so the next step (of this or
-//    the next task) is in flight while the current one is dequantised and
-//    multiplied.  The step's groups are worked on together, with independent
-//    fp16 chains, to keep the issue slots busy.  No staging barriers.
+//  * Each warp owns a shared-memory buffer and an mbarrier.  A task's rows
+//    are contiguous in every packed tensor, so lane 0 fetches the whole task
+//    (codes, scales, zero words of its gate and up rows, or of its down
+//    rows) with a handful of bulk asynchronous copies; the warp's lanes then
+//    dequantise from shared memory.  With 14 warps per SM that many tasks are
+//    in flight at once, without spending registers on them.  The kGPI groups
+//    of a row are worked on together, with independent fp16 chains, to keep
+//    the issue slots busy.
 //  * Dequantisation and arithmetic are those of common.cuh: code - zero in
 //    fp16 pairs, fp16 products summed per group, fp32 group accumulation.
 //  * Step 4 writes each pair's fp32 projection to the workspace and counts
@@ -30,11 +32,11 @@
 
 namespace moe {
 
-constexpr int kDecWarps = 16;
+constexpr int kDecWarps = 14;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecMaxT = 8;   // decode batches: T <= 8
 constexpr int kDecPass = 4;   // activation rows per compute pass
-constexpr int kGPI = 2;       // groups per lane per pipeline step
+constexpr int kGPI = 2;       // groups per lane worked on together
 
 enum { kDecGateUp = 0, kDecDown = 1 };
 
@@ -54,18 +56,71 @@ struct DecodeArgs {
     uint32_t *counters;  // step 4: [H/8]
     uint32_t *err;
     int slots;           // activation rows held in shared memory
+    uint32_t wbytes;     // per-warp task buffer
 };
+
+// Per-warp buffer for a task of RT rows in each of nmat matrices: codes,
+// then scales, then zero words of every matrix; scale and zero copies are
+// widened to 16-byte boundaries, hence the slack.
+struct WarpGeom {
+    uint32_t q_bytes, s_bytes, z_bytes, bytes;
+};
+
+__host__ __device__ inline WarpGeom warp_geom(int RT, int nmat, int K) {
+    const int G = K / 32;
+    WarpGeom g;
+    g.q_bytes = (uint32_t)(RT * K / 2);
+    g.s_bytes = (uint32_t)align_up((size_t)RT * G * 2 + 32, 16);
+    g.z_bytes = (uint32_t)align_up((size_t)(RT / 8 + 2) * G * 4 + 32, 16);
+    g.bytes = (uint32_t)align_up((size_t)nmat * (g.q_bytes + g.s_bytes + g.z_bytes), 128);
+    return g;
+}
 
 struct DecLayout {
-    uint32_t meta, xc, total;
+    uint32_t meta, xc, wbuf, bars, total;
 };
 
-__host__ __device__ inline DecLayout dec_layout(int E, int P, int slots, int K) {
+__host__ __device__ inline DecLayout dec_layout(int E, int P, int slots, int K, uint32_t wbytes) {
     DecLayout L;
     L.meta = 0;
     L.xc = (uint32_t)align_up((size_t)(4 + E + E + 1 + P) * 4, 128);
-    L.total = L.xc + (uint32_t)align_up((size_t)slots * K * 2, 128);
+    L.wbuf = L.xc + (uint32_t)align_up((size_t)slots * K * 2, 128);
+    L.bars = L.wbuf + (uint32_t)kDecWarps * wbytes;
+    L.total = L.bars + kDecWarps * 8;
     return L;
+}
+
+// Byte ranges (from the tensor bases) of one matrix block of a task: rows
+// [n_first, n_first + cnt) of expert e; scale and zero ranges widened to
+// 16-byte boundaries (the tensors' sizes are multiples of 16 bytes).
+struct WarpCopy {
+    size_t q_off;
+    uint32_t q_len;
+    uint32_t s_skip;   // bytes from the copied scale range's start to the first row
+    size_t s_a;
+    uint32_t s_len;
+    uint32_t z_skip;
+    size_t z_a;
+    uint32_t z_len;
+};
+
+__device__ __forceinline__ WarpCopy warp_copy(int e, int n_first, int cnt, int N, int K) {
+    const int G = K / 32;
+    WarpCopy c;
+    const size_t row = (size_t)e * N + n_first;
+    c.q_off = row * (size_t)(K / 2);
+    c.q_len = (uint32_t)(cnt * (K / 2));
+    const size_t s_lo = row * G * 2, s_hi = (row + cnt) * G * 2;
+    c.s_a = s_lo & ~(size_t)15;
+    c.s_skip = (uint32_t)(s_lo - c.s_a);
+    c.s_len = (uint32_t)(align_up(s_hi, 16) - c.s_a);
+    const size_t zr0 = (size_t)e * (N / 8) + n_first / 8;
+    const size_t zr1 = (size_t)e * (N / 8) + (n_first + cnt - 1) / 8;
+    const size_t z_lo = zr0 * G * 4;
+    c.z_a = z_lo & ~(size_t)15;
+    c.z_skip = (uint32_t)(z_lo - c.z_a);
+    c.z_len = (uint32_t)(align_up((zr1 + 1) * G * 4, 16) - c.z_a);
+    return c;
 }
 
 // shared activation cache: slot s, 8-element block kb = 4*g + wd stored at
@@ -78,22 +133,6 @@ __device__ __forceinline__ uint32_t dec_word(const uint4 &w, int i) {
     return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
 }
 
-// Position of a warp in its work list: task u (RT row units of expert e
-// from unit0), token pass tb (activation rows r0+tb .. r0+tb+3) and group
-// step gs (groups gs*L*kGPI + ks + L*i, i < kGPI, of every row).
-struct Cursor {
-    int u, e, unit0, r0, ne, tb, gs;
-};
-
-// Registers of one load step: per row unit, matrix and group, the 16-byte
-// code word, the scale and the packed zero word.
-template <int RU, int NMAT>
-struct Step {
-    uint4 w[RU][NMAT][kGPI];
-    float sc[RU][NMAT][kGPI];
-    uint32_t zw[RU][NMAT][kGPI];
-};
-
 template <int MODE, int L, int RU>
 struct DecTraits {
     static constexpr int nmat = MODE == kDecGateUp ? 2 : 1;
@@ -101,84 +140,24 @@ struct DecTraits {
     static constexpr int RT = UPW * RU; // row units per task
 };
 
-// Moves c to the first valid task at or after u (c.u = t1 when none is left).
-template <int MODE, int L, int RU>
-__device__ __forceinline__ void cursor_task(Cursor &c, int u, int t1, int TPE, const int *s_active,
-                                            const int *s_offs, const DecodeArgs &a, int lane) {
-    for (; u < t1; ++u) {
-        const int ai = u / TPE;
-        const int e = s_active[ai];
-        if (e >= 0 && e < a.E) {
-            const int r0 = s_offs[e], r1 = s_offs[e + 1];
-            if (r0 >= 0 && r1 <= a.P && r1 > r0) {
-                c.u = u;
-                c.e = e;
-                c.unit0 = (u - ai * TPE) * DecTraits<MODE, L, RU>::RT;
-                c.r0 = r0;
-                c.ne = r1 - r0;
-                c.tb = 0;
-                c.gs = 0;
-                return;
-            }
-        }
-        if (lane == 0) set_error(a.err, MOE_DEVERR_BAD_METADATA);
-    }
-    c.u = t1;
-}
+// The task a warp works on: RT row units of expert e from unit0, and the
+// token pass tb (activation rows r0+tb .. r0+tb+3 of the segment).
+struct Cursor {
+    int e, unit0, cnt, r0, ne, tb;
+};
 
-template <int MODE, int L, int RU>
-__device__ __forceinline__ void cursor_next(Cursor &c, int t1, int TPE, int nsteps, const int *s_active,
-                                            const int *s_offs, const DecodeArgs &a, int lane) {
-    if (++c.gs < nsteps) return;
-    c.gs = 0;
-    c.tb += kDecPass;
-    if (c.tb < c.ne) return;
-    cursor_task<MODE, L, RU>(c, c.u + 1, t1, TPE, s_active, s_offs, a, lane);
-}
-
-// Issue every load of the step at cursor c.  Groups past G and rows past
-// the expert load nothing: zero codes, zero point 0 and scale 0.
-template <int MODE, int L, int RU>
-__device__ __forceinline__ void dec_issue(Step<RU, DecTraits<MODE, L, RU>::nmat> &st, const Cursor &c,
-                                          const DecodeArgs &a, int lane) {
-    using Tr = DecTraits<MODE, L, RU>;
-    const int G = a.K / 32, KW = a.K / 8;
-    const int ks = lane % L, us = lane / L;
-#pragma unroll
-    for (int ru = 0; ru < RU; ++ru) {
-        const int unit = c.unit0 + us + ru * Tr::UPW;
-#pragma unroll
-        for (int b = 0; b < Tr::nmat; ++b) {
-            const int n = unit + b * a.rows;  // matrix row
-            const size_t row = (size_t)c.e * a.N + n;
-            const uint4 *qp = reinterpret_cast<const uint4 *>(a.q + row * KW);
-            const __half *sp = a.s + row * G;
-            const uint32_t *zp = a.z + ((size_t)c.e * (a.N / 8) + n / 8) * G;
-#pragma unroll
-            for (int i = 0; i < kGPI; ++i) {
-                const int g = c.gs * L * kGPI + ks + L * i;
-                const bool ok = unit < a.rows && g < G;
-                st.w[ru][b][i] = ok ? ldg_stream(qp + g) : make_uint4(0, 0, 0, 0);
-                st.sc[ru][b][i] = ok ? __half2float(__ldg(sp + g)) : 0.f;
-                st.zw[ru][b][i] = ok ? __ldg(zp + g) : 0u;
-            }
-        }
-    }
-}
-
-// Dequantise the step at cursor c and accumulate against NT activation rows.
-// The kGPI groups of every row are worked on together, each product sum in
-// up to four independent fp16 chains, to keep enough independent
-// instructions in flight.
+// Dequantise the warp's buffered task and accumulate against NT activation
+// rows.  The kGPI groups of every row are worked on together, each product
+// sum in up to four independent fp16 chains.
 template <int MODE, int L, int RU, int NT>
-__device__ __forceinline__ void dec_compute(const Step<RU, DecTraits<MODE, L, RU>::nmat> &st,
+__device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &wg,
                                             float (&acc)[RU][DecTraits<MODE, L, RU>::nmat][kDecPass],
                                             const Cursor &c, const int *s_pairs, const uint8_t *xcb,
                                             int hbase, bool hc, const DecodeArgs &a, int lane) {
     using Tr = DecTraits<MODE, L, RU>;
     constexpr int nmat = Tr::nmat;
     constexpr int CH = NT == 1 ? 4 : (NT == 2 ? 2 : 1);  // independent chains per product sum
-    const int K = a.K, G = K / 32;
+    const int K = a.K, G = K / 32, GL = (G + L - 1) / L;
     const int ks = lane % L, us = lane / L;
     uint32_t xrow[NT];  // byte offset of each activation row in the cache
 #pragma unroll
@@ -188,69 +167,99 @@ __device__ __forceinline__ void dec_compute(const Step<RU, DecTraits<MODE, L, RU
         const int slot = MODE == kDecGateUp ? ((p >= 0 && p < a.P) ? p / a.k : 0) : r - hbase;
         xrow[t] = (uint32_t)(slot * 4 * G * 16);
     }
+    // where each matrix block's scales and zero words start in the buffer
+    uint32_t soff[nmat], zoff[nmat];
+    int nfirst[nmat];
+#pragma unroll
+    for (int b = 0; b < nmat; ++b) {
+        nfirst[b] = c.unit0 + b * a.rows;
+        const WarpCopy cp = warp_copy(c.e, nfirst[b], c.cnt, a.N, K);
+        soff[b] = nmat * wg.q_bytes + b * wg.s_bytes + cp.s_skip;
+        zoff[b] = nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes + cp.z_skip;
+    }
 #pragma unroll
     for (int ru = 0; ru < RU; ++ru) {
-        const int unit = c.unit0 + us + ru * Tr::UPW;
-        ZeroPoint zp[nmat][kGPI];
-#pragma unroll
-        for (int b = 0; b < nmat; ++b)
-#pragma unroll
-            for (int i = 0; i < kGPI; ++i)
-                zp[b][i] = make_zero_point((st.zw[ru][b][i] >> (4 * ((unit + b * a.rows) & 7))) & 0xFu);
-        __half2 hs[kGPI][nmat][NT][CH];
-#pragma unroll
-        for (int i = 0; i < kGPI; ++i)
-#pragma unroll
-            for (int b = 0; b < nmat; ++b)
-#pragma unroll
-                for (int t = 0; t < NT; ++t)
-#pragma unroll
-                    for (int ch = 0; ch < CH; ++ch) hs[i][b][t][ch] = __float2half2_rn(0.f);
-#pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
+        const int lr = us + ru * Tr::UPW;  // row within the task
+        if (lr >= c.cnt) continue;
+        for (int m0 = 0; m0 < GL; m0 += kGPI) {
+            uint4 w[nmat][kGPI];
+            float sc[nmat][kGPI];
+            ZeroPoint zp[nmat][kGPI];
 #pragma unroll
             for (int i = 0; i < kGPI; ++i) {
-                const int g = c.gs * L * kGPI + ks + L * i;
+                const int g = ks + L * (m0 + i);
                 const bool gok = g < G;
-                __half2 dq[nmat][4];
 #pragma unroll
-                for (int b = 0; b < nmat; ++b) dequant_word(dec_word(st.w[ru][b][i], wd), zp[b][i], dq[b]);
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    // groups past G have zero codes and scale 0; their
-                    // activations read as zero so the sums stay finite
-                    uint4 X = make_uint4(0, 0, 0, 0);
+                for (int b = 0; b < nmat; ++b) {
+                    const int n = nfirst[b] + lr;
                     if (gok) {
-                        if (MODE == kDecGateUp || hc) {
-                            X = *reinterpret_cast<const uint4 *>(xcb + xrow[t] + (uint32_t)((wd * G + g) * 16));
-                        } else {
-                            X = pair_interleave(__ldg(reinterpret_cast<const uint4 *>(
-                                a.vin + (size_t)(c.r0 + c.tb + t) * K + g * 32 + wd * 8)));
-                        }
-                    }
-#pragma unroll
-                    for (int b = 0; b < nmat; ++b) {
-                        __half2 &h = hs[i][b][t][wd % CH];
-                        h = __hfma2(dq[b][0], u32_as_half2(X.x), h);
-                        h = __hfma2(dq[b][1], u32_as_half2(X.y), h);
-                        h = __hfma2(dq[b][2], u32_as_half2(X.z), h);
-                        h = __hfma2(dq[b][3], u32_as_half2(X.w), h);
+                        w[b][i] = *reinterpret_cast<const uint4 *>(wb + b * wg.q_bytes + lr * (K / 2) + g * 16);
+                        sc[b][i] = __half2float(
+                            *reinterpret_cast<const __half *>(wb + soff[b] + (lr * G + g) * 2));
+                        const uint32_t zw = *reinterpret_cast<const uint32_t *>(
+                            wb + zoff[b] + ((n / 8 - nfirst[b] / 8) * G + g) * 4);
+                        zp[b][i] = make_zero_point((zw >> (4 * (n & 7))) & 0xFu);
+                    } else {
+                        // groups past G: zero codes, zero point 0, scale 0
+                        w[b][i] = make_uint4(0, 0, 0, 0);
+                        sc[b][i] = 0.f;
+                        zp[b][i] = make_zero_point(0u);
                     }
                 }
             }
-        }
+            __half2 hs[kGPI][nmat][NT][CH];
 #pragma unroll
-        for (int i = 0; i < kGPI; ++i)
+            for (int i = 0; i < kGPI; ++i)
 #pragma unroll
-            for (int b = 0; b < nmat; ++b)
+                for (int b = 0; b < nmat; ++b)
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    __half2 s2 = hs[i][b][t][0];
+                    for (int t = 0; t < NT; ++t)
 #pragma unroll
-                    for (int ch = 1; ch < CH; ++ch) s2 = __hadd2(s2, hs[i][b][t][ch]);
-                    const float2 f = __half22float2(s2);
-                    acc[ru][b][t] = fmaf(st.sc[ru][b][i], f.x + f.y, acc[ru][b][t]);
+                        for (int ch = 0; ch < CH; ++ch) hs[i][b][t][ch] = __float2half2_rn(0.f);
+#pragma unroll
+            for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+                for (int i = 0; i < kGPI; ++i) {
+                    const int g = ks + L * (m0 + i);
+                    __half2 dq[nmat][4];
+#pragma unroll
+                    for (int b = 0; b < nmat; ++b) dequant_word(dec_word(w[b][i], wd), zp[b][i], dq[b]);
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        // activations of groups past G read as zero so sums stay finite
+                        uint4 X = make_uint4(0, 0, 0, 0);
+                        if (g < G) {
+                            if (MODE == kDecGateUp || hc) {
+                                X = *reinterpret_cast<const uint4 *>(xcb + xrow[t] + (uint32_t)((wd * G + g) * 16));
+                            } else {
+                                X = pair_interleave(__ldg(reinterpret_cast<const uint4 *>(
+                                    a.vin + (size_t)(c.r0 + c.tb + t) * K + g * 32 + wd * 8)));
+                            }
+                        }
+#pragma unroll
+                        for (int b = 0; b < nmat; ++b) {
+                            __half2 &h = hs[i][b][t][wd % CH];
+                            h = __hfma2(dq[b][0], u32_as_half2(X.x), h);
+                            h = __hfma2(dq[b][1], u32_as_half2(X.y), h);
+                            h = __hfma2(dq[b][2], u32_as_half2(X.z), h);
+                            h = __hfma2(dq[b][3], u32_as_half2(X.w), h);
+                        }
+                    }
                 }
+            }
+#pragma unroll
+            for (int i = 0; i < kGPI; ++i)
+#pragma unroll
+                for (int b = 0; b < nmat; ++b)
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        __half2 s2 = hs[i][b][t][0];
+#pragma unroll
+                        for (int ch = 1; ch < CH; ++ch) s2 = __hadd2(s2, hs[i][b][t][ch]);
+                        const float2 f = __half22float2(s2);
+                        acc[ru][b][t] = fmaf(sc[b][i], f.x + f.y, acc[ru][b][t]);
+                    }
+        }
     }
 }
 
@@ -331,34 +340,6 @@ __device__ __forceinline__ void dec_combine(int n_lo, int n_hi, int A, const Dec
     }
 }
 
-// compute + (at the end of a pass) finish + (at the end of a task) combine
-// for the step at cursor c
-template <int MODE, int L, int RU>
-__device__ __forceinline__ void dec_consume(const Step<RU, DecTraits<MODE, L, RU>::nmat> &st,
-                                            float (&acc)[RU][DecTraits<MODE, L, RU>::nmat][kDecPass],
-                                            const Cursor &c, int nsteps, const int *s_pairs,
-                                            const uint8_t *xcb, int hbase, bool hcached, int A,
-                                            const DecodeArgs &a, int lane) {
-    using Tr = DecTraits<MODE, L, RU>;
-    const int nt = min(kDecPass, c.ne - c.tb);
-    const bool hc = hcached && c.r0 >= hbase && c.r0 + c.ne - hbase <= a.slots;
-    switch (nt) {
-        case 1: dec_compute<MODE, L, RU, 1>(st, acc, c, s_pairs, xcb, hbase, hc, a, lane); break;
-        case 2: dec_compute<MODE, L, RU, 2>(st, acc, c, s_pairs, xcb, hbase, hc, a, lane); break;
-        case 3: dec_compute<MODE, L, RU, 3>(st, acc, c, s_pairs, xcb, hbase, hc, a, lane); break;
-        default: dec_compute<MODE, L, RU, 4>(st, acc, c, s_pairs, xcb, hbase, hc, a, lane); break;
-    }
-    if (c.gs + 1 < nsteps) return;
-    switch (nt) {
-        case 1: dec_finish<MODE, L, RU, 1>(acc, c, s_pairs, a, lane); break;
-        case 2: dec_finish<MODE, L, RU, 2>(acc, c, s_pairs, a, lane); break;
-        case 3: dec_finish<MODE, L, RU, 3>(acc, c, s_pairs, a, lane); break;
-        default: dec_finish<MODE, L, RU, 4>(acc, c, s_pairs, a, lane); break;
-    }
-    if (MODE == kDecDown && c.tb + kDecPass >= c.ne)
-        dec_combine(c.unit0, min(c.unit0 + Tr::RT, a.rows), A, a, lane);
-}
-
 // Cooperative copy of n activation rows (starting at src) into cache slots
 // 0..n-1, pair-interleaved; every thread issues its loads before any store.
 __device__ __forceinline__ void dec_stage_rows(const __half *src, int n, int K, int G, uint8_t *xcb,
@@ -385,14 +366,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
     constexpr int nmat = Tr::nmat;
     extern __shared__ __align__(128) uint8_t smem[];
     const int K = a.K, G = K / 32;
-    const DecLayout Ly = dec_layout(a.E, a.P, a.slots, K);
+    const DecLayout Ly = dec_layout(a.E, a.P, a.slots, K, a.wbytes);
+    const WarpGeom wg = warp_geom(Tr::RT, nmat, K);
     int *s_meta = reinterpret_cast<int *>(smem + Ly.meta);
     int *s_active = s_meta + 4;
     int *s_offs = s_active + a.E;
     int *s_pairs = s_offs + a.E + 1;
     uint8_t *xcb = smem + Ly.xc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *wb = smem + Ly.wbuf + (size_t)warp * a.wbytes;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp;
 
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
     pdl_wait();
     pdl_trigger();
 
@@ -430,13 +418,51 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
     const long long NW = (long long)gridDim.x * kDecWarps;
     const long long gw = (long long)blockIdx.x * kDecWarps + warp;
     const int t0 = (int)(U * gw / NW), t1 = (int)(U * (gw + 1) / NW);
-    const int nsteps = (G + L * kGPI - 1) / (L * kGPI);  // group steps per row
 
-    // the first step of this warp goes out before anything else is waited for
+    // task u's expert and segment; false (and flagged) if the metadata is bad
+    auto task = [&](int u, Cursor &c) -> bool {
+        const int ai = u / TPE;
+        c.e = s_active[ai];
+        if (c.e < 0 || c.e >= a.E) return false;
+        c.r0 = s_offs[c.e];
+        const int r1 = s_offs[c.e + 1];
+        if (c.r0 < 0 || r1 > a.P || r1 <= c.r0) return false;
+        c.ne = r1 - c.r0;
+        c.unit0 = (u - ai * TPE) * Tr::RT;
+        c.cnt = min(Tr::RT, a.rows - c.unit0);
+        c.tb = 0;
+        return true;
+    };
+    // lane 0 fetches the whole task into this warp's buffer
+    auto issue = [&](const Cursor &c) {
+        if (lane != 0) return;
+        fence_proxy_async();  // this warp's earlier reads of the buffer come first
+        WarpCopy cp[nmat];
+        uint32_t tx = 0;
+#pragma unroll
+        for (int b = 0; b < nmat; ++b) {
+            cp[b] = warp_copy(c.e, c.unit0 + b * a.rows, c.cnt, a.N, K);
+            tx += cp[b].q_len + cp[b].s_len + cp[b].z_len;
+        }
+        mbar_arrive_expect_tx(bar, tx);
+#pragma unroll
+        for (int b = 0; b < nmat; ++b) {
+            bulk_g2s(wb + b * wg.q_bytes, reinterpret_cast<const uint8_t *>(a.q) + cp[b].q_off, cp[b].q_len, bar);
+            bulk_g2s(wb + nmat * wg.q_bytes + b * wg.s_bytes, reinterpret_cast<const uint8_t *>(a.s) + cp[b].s_a,
+                     cp[b].s_len, bar);
+            bulk_g2s(wb + nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes,
+                     reinterpret_cast<const uint8_t *>(a.z) + cp[b].z_a, cp[b].z_len, bar);
+        }
+    };
+
+    // the first task of this warp goes out before anything else is waited for
+    int u = t0;
     Cursor cur;
-    cursor_task<MODE, L, RU>(cur, t0, t1, TPE, s_active, s_offs, a, lane);
-    Step<RU, nmat> bA, bB;
-    if (cur.u < t1) dec_issue<MODE, L, RU>(bA, cur, a, lane);
+    while (u < t1 && !task(u, cur)) {
+        if (lane == 0) set_error(a.err, MOE_DEVERR_BAD_METADATA);
+        ++u;
+    }
+    if (u < t1) issue(cur);
 
     // ---- step 4: cache the h rows of every segment this CTA touches
     int hbase = 0;
@@ -458,7 +484,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         __syncthreads();
     }
 
-    // ---- one-step-ahead register pipeline over this warp's work
     float acc[RU][nmat][kDecPass];
 #pragma unroll
     for (int ru = 0; ru < RU; ++ru)
@@ -466,24 +491,52 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         for (int b = 0; b < nmat; ++b)
 #pragma unroll
             for (int t = 0; t < kDecPass; ++t) acc[ru][b][t] = 0.f;
-    while (cur.u < t1) {
-        Cursor nxt = cur;
-        cursor_next<MODE, L, RU>(nxt, t1, TPE, nsteps, s_active, s_offs, a, lane);
-        if (nxt.u < t1) dec_issue<MODE, L, RU>(bB, nxt, a, lane);
-        dec_consume<MODE, L, RU>(bA, acc, cur, nsteps, s_pairs, xcb, hbase, hcached, A, a, lane);
-        if (nxt.u >= t1) break;
-        cur = nxt;
-        cursor_next<MODE, L, RU>(nxt, t1, TPE, nsteps, s_active, s_offs, a, lane);
-        if (nxt.u < t1) dec_issue<MODE, L, RU>(bA, nxt, a, lane);
-        dec_consume<MODE, L, RU>(bB, acc, cur, nsteps, s_pairs, xcb, hbase, hcached, A, a, lane);
-        cur = nxt;
+    uint32_t phase = 0;
+    while (u < t1) {
+        if (!mbar_wait_bounded(bar, phase, nullptr)) {
+            if (lane == 0) set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
+            mbar_wait_bounded(bar, phase, nullptr);  // never leave with a copy in flight
+            return;
+        }
+        phase ^= 1u;
+        const bool hc = hcached && cur.r0 >= hbase && cur.r0 + cur.ne - hbase <= a.slots;
+        // segments longer than a pass (several tokens on one expert) take more passes
+        for (cur.tb = 0; cur.tb < cur.ne; cur.tb += kDecPass) {
+            const int nt = min(kDecPass, cur.ne - cur.tb);
+            switch (nt) {
+                case 1:
+                    dec_compute<MODE, L, RU, 1>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_finish<MODE, L, RU, 1>(acc, cur, s_pairs, a, lane);
+                    break;
+                case 2:
+                    dec_compute<MODE, L, RU, 2>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_finish<MODE, L, RU, 2>(acc, cur, s_pairs, a, lane);
+                    break;
+                case 3:
+                    dec_compute<MODE, L, RU, 3>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_finish<MODE, L, RU, 3>(acc, cur, s_pairs, a, lane);
+                    break;
+                default:
+                    dec_compute<MODE, L, RU, 4>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_finish<MODE, L, RU, 4>(acc, cur, s_pairs, a, lane);
+                    break;
+            }
+        }
+        if (MODE == kDecDown) dec_combine(cur.unit0, cur.unit0 + cur.cnt, A, a, lane);
+        __syncwarp();
+        // next valid task
+        for (++u; u < t1 && !task(u, cur); ++u)
+            if (lane == 0) set_error(a.err, MOE_DEVERR_BAD_METADATA);
+        if (u < t1) issue(cur);
     }
 }
 
 // ---------------------------------------------------------------- launchers
 template <int MODE, int L, int RU>
 static cudaError_t launch_decode_t(DecodeArgs a, int num_sms, size_t smem_limit, cudaStream_t stream) {
-    const size_t smem = dec_layout(a.E, a.P, a.slots, a.K).total;
+    using Tr = DecTraits<MODE, L, RU>;
+    a.wbytes = warp_geom(Tr::RT, Tr::nmat, a.K).bytes;
+    const size_t smem = dec_layout(a.E, a.P, a.slots, a.K, a.wbytes).total;
     if (smem > smem_limit) return cudaErrorInvalidConfiguration;
     static int configured[128];
     cudaError_t e = ensure_smem(decode_kernel<MODE, L, RU>, configured, smem);
@@ -494,10 +547,21 @@ static cudaError_t launch_decode_t(DecodeArgs a, int num_sms, size_t smem_limit,
 // Lanes per row unit: a power of two giving each lane about five groups.
 static int lanes_for(int G) { return G >= 40 ? 8 : (G >= 20 ? 4 : (G >= 10 ? 2 : 1)); }
 
+
+static int lanes_for(int G);
+
+// Largest per-warp buffer the decode kernels need for these sizes (step 3:
+// one task of 32/L row pairs; step 4: one task of 2*32/L rows).
+static uint32_t decode_wbytes(int H, int I, bool gate_up) {
+    const int G = (gate_up ? H : I) / 32, L = lanes_for(G);
+    return gate_up ? warp_geom(32 / L, 2, H).bytes : warp_geom(2 * (32 / L), 1, I).bytes;
+}
+
 bool decode_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int P = T * k;
-    return T >= 1 && T <= kDecMaxT && dec_layout(E, P, T, H).total <= smem_limit &&
-           dec_layout(E, P, 4 * T, I).total <= smem_limit;
+    return T >= 1 && T <= kDecMaxT &&
+           dec_layout(E, P, T, H, decode_wbytes(H, I, true)).total <= smem_limit &&
+           dec_layout(E, P, 4 * T, I, decode_wbytes(H, I, false)).total <= smem_limit;
 }
 
 cudaError_t launch_gate_up_decode(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
