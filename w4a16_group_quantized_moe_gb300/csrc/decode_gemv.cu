@@ -9,12 +9,12 @@
 //
 //  * One 14-warp CTA per SM.  A prologue, run by every thread with all loads
 //    issued before any store, brings the routing metadata (active list,
-//    offsets, pair ids) and, in step 3, every x row into shared memory in a
-//    single round trip.  Step 4 caches the h rows of the CTA's segments (one
-//    contiguous run of sorted rows) the same way.
+//    offsets, pair ids) and the activations (every x row in step 3, every h
+//    row in step 4 when they fit) into shared memory in a single round trip.
 //  * Work is cut into warp tasks: RT consecutive row units (gate/up row pairs
 //    in step 3, output rows in step 4) of one active expert, L lanes per row
-//    unit.  Task lists are split into equal contiguous ranges per warp.
+//    unit.  Tasks are dealt round-robin over CTAs, then over their warps, so
+//    every SM gets the same share whatever the active experts.
 //  * Each warp owns a shared-memory buffer and an mbarrier.  A task's rows
 //    are contiguous in every packed tensor, so lane 0 fetches the whole task
 //    (codes, scales, zero words of its gate and up rows, or of its down
@@ -25,9 +25,14 @@
 //    the issue slots busy.
 //  * Dequantisation and arithmetic are those of common.cuh: code - zero in
 //    fp16 pairs, fp16 products summed per group, fp32 group accumulation.
+//  * For the geometries the layer is specified on, the number of groups per
+//    row is a compile-time constant, so every shared-memory offset of a
+//    task is an immediate and each lane's group loop unrolls completely.
 //  * Step 4 writes each pair's fp32 projection to the workspace and counts
-//    finished rows per 8-row output block; the warp that completes a block
-//    sums the block's k terms per token in order and writes fp16.
+//    finished rows per 8-row output block in shared memory.  At the end each
+//    CTA publishes its counts (one fence, parallel atomics); whichever CTA
+//    completes a block sums the block's k terms per token in order and writes
+//    fp16 (deterministic, no extra launch).
 #include "common.cuh"
 
 namespace moe {
@@ -55,7 +60,8 @@ struct DecodeArgs {
     __half *out;         // step 4: [T][H]
     uint32_t *counters;  // step 4: [H/8]
     uint32_t *err;
-    int slots;           // activation rows held in shared memory
+    int slots;           // activation rows held in shared memory (step 4: P or 0)
+    int nblk;            // step 4: 8-row output blocks (H/8); step 3: 0
     uint32_t wbytes;     // per-warp task buffer
 };
 
@@ -76,14 +82,18 @@ __host__ __device__ inline WarpGeom warp_geom(int RT, int nmat, int K) {
     return g;
 }
 
+// meta: [A | pad3 | active E | offsets E+1 | pairs P] ints; blk: 2*nblk ints
+// (per-block row counts, then the list of blocks this CTA completed); xc:
+// activation cache; wbuf: per-warp task buffers; bars: per-warp mbarriers.
 struct DecLayout {
-    uint32_t meta, xc, wbuf, bars, total;
+    uint32_t meta, blk, xc, wbuf, bars, total;
 };
 
-__host__ __device__ inline DecLayout dec_layout(int E, int P, int slots, int K, uint32_t wbytes) {
+__host__ __device__ inline DecLayout dec_layout(int E, int P, int nblk, int slots, int K, uint32_t wbytes) {
     DecLayout L;
     L.meta = 0;
-    L.xc = (uint32_t)align_up((size_t)(4 + E + E + 1 + P) * 4, 128);
+    L.blk = (uint32_t)align_up((size_t)(4 + E + E + 1 + P) * 4, 128);
+    L.xc = L.blk + (uint32_t)align_up((size_t)(2 * nblk + 4) * 4, 128);
     L.wbuf = L.xc + (uint32_t)align_up((size_t)slots * K * 2, 128);
     L.bars = L.wbuf + (uint32_t)kDecWarps * wbytes;
     L.total = L.bars + kDecWarps * 8;
@@ -147,27 +157,29 @@ struct Cursor {
 };
 
 // Dequantise the warp's buffered task and accumulate against NT activation
-// rows.  The kGPI groups of every row are worked on together, each product
-// sum in up to four independent fp16 chains.
-template <int MODE, int L, int RU, int NT>
+// rows.  GT = groups per row when known at compile time (0: read from a.K).
+// The kGPI groups of a step are worked on together, each product sum in up
+// to four independent fp16 chains.
+template <int MODE, int L, int RU, int GT, int NT>
 __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &wg,
                                             float (&acc)[RU][DecTraits<MODE, L, RU>::nmat][kDecPass],
                                             const Cursor &c, const int *s_pairs, const uint8_t *xcb,
-                                            int hbase, bool hc, const DecodeArgs &a, int lane) {
+                                            bool hc, const DecodeArgs &a, int lane) {
     using Tr = DecTraits<MODE, L, RU>;
     constexpr int nmat = Tr::nmat;
     constexpr int CH = NT == 1 ? 4 : (NT == 2 ? 2 : 1);  // independent chains per product sum
-    const int K = a.K, G = K / 32, GL = (G + L - 1) / L;
+    const int G = GT ? GT : a.K / 32;
+    const int K = 32 * G;
+    const int GL = (G + L - 1) / L;  // groups per lane (compile time when GT != 0)
     const int ks = lane % L, us = lane / L;
-    uint32_t xrow[NT];  // byte offset of each activation row in the cache
+    const uint8_t *xb[NT];  // this lane's first block of each activation row
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const int r = c.r0 + c.tb + t;
         const int p = s_pairs[r];
-        const int slot = MODE == kDecGateUp ? ((p >= 0 && p < a.P) ? p / a.k : 0) : r - hbase;
-        xrow[t] = (uint32_t)(slot * 4 * G * 16);
+        const int slot = MODE == kDecGateUp ? ((p >= 0 && p < a.P) ? p / a.k : 0) : r;
+        xb[t] = xcb + (size_t)slot * 4 * G * 16 + ks * 16;
     }
-    // where each matrix block's scales and zero words start in the buffer
     uint32_t soff[nmat], zoff[nmat];
     int nfirst[nmat];
 #pragma unroll
@@ -181,29 +193,39 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
     for (int ru = 0; ru < RU; ++ru) {
         const int lr = us + ru * Tr::UPW;  // row within the task
         if (lr >= c.cnt) continue;
+        const uint8_t *qp[nmat], *sp[nmat], *zp[nmat];
+        uint32_t zsh[nmat];
+#pragma unroll
+        for (int b = 0; b < nmat; ++b) {
+            const int n = nfirst[b] + lr;
+            qp[b] = wb + b * wg.q_bytes + lr * (K / 2) + ks * 16;
+            sp[b] = wb + soff[b] + (lr * G + ks) * 2;
+            zp[b] = wb + zoff[b] + ((n / 8 - nfirst[b] / 8) * G + ks) * 4;
+            zsh[b] = 4 * (n & 7);
+        }
+#pragma unroll
         for (int m0 = 0; m0 < GL; m0 += kGPI) {
             uint4 w[nmat][kGPI];
             float sc[nmat][kGPI];
-            ZeroPoint zp[nmat][kGPI];
+            ZeroPoint zq[nmat][kGPI];
+            bool gok[kGPI];
 #pragma unroll
             for (int i = 0; i < kGPI; ++i) {
-                const int g = ks + L * (m0 + i);
-                const bool gok = g < G;
+                const int m = m0 + i;
+                // with G a multiple of L (and GT known) this folds to a constant
+                gok[i] = (GT && GT % L == 0) ? m < GL : ks + L * m < G;
 #pragma unroll
                 for (int b = 0; b < nmat; ++b) {
-                    const int n = nfirst[b] + lr;
-                    if (gok) {
-                        w[b][i] = *reinterpret_cast<const uint4 *>(wb + b * wg.q_bytes + lr * (K / 2) + g * 16);
-                        sc[b][i] = __half2float(
-                            *reinterpret_cast<const __half *>(wb + soff[b] + (lr * G + g) * 2));
-                        const uint32_t zw = *reinterpret_cast<const uint32_t *>(
-                            wb + zoff[b] + ((n / 8 - nfirst[b] / 8) * G + g) * 4);
-                        zp[b][i] = make_zero_point((zw >> (4 * (n & 7))) & 0xFu);
+                    if (gok[i]) {
+                        w[b][i] = *reinterpret_cast<const uint4 *>(qp[b] + L * 16 * m);
+                        sc[b][i] = __half2float(*reinterpret_cast<const __half *>(sp[b] + L * 2 * m));
+                        zq[b][i] = make_zero_point(
+                            (*reinterpret_cast<const uint32_t *>(zp[b] + L * 4 * m) >> zsh[b]) & 0xFu);
                     } else {
                         // groups past G: zero codes, zero point 0, scale 0
                         w[b][i] = make_uint4(0, 0, 0, 0);
                         sc[b][i] = 0.f;
-                        zp[b][i] = make_zero_point(0u);
+                        zq[b][i] = make_zero_point(0u);
                     }
                 }
             }
@@ -220,18 +242,19 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
             for (int wd = 0; wd < 4; ++wd) {
 #pragma unroll
                 for (int i = 0; i < kGPI; ++i) {
-                    const int g = ks + L * (m0 + i);
+                    const int m = m0 + i;
                     __half2 dq[nmat][4];
 #pragma unroll
-                    for (int b = 0; b < nmat; ++b) dequant_word(dec_word(w[b][i], wd), zp[b][i], dq[b]);
+                    for (int b = 0; b < nmat; ++b) dequant_word(dec_word(w[b][i], wd), zq[b][i], dq[b]);
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         // activations of groups past G read as zero so sums stay finite
                         uint4 X = make_uint4(0, 0, 0, 0);
-                        if (g < G) {
+                        if (gok[i]) {
                             if (MODE == kDecGateUp || hc) {
-                                X = *reinterpret_cast<const uint4 *>(xcb + xrow[t] + (uint32_t)((wd * G + g) * 16));
+                                X = *reinterpret_cast<const uint4 *>(xb[t] + (wd * G + L * m) * 16);
                             } else {
+                                const int g = ks + L * m;
                                 X = pair_interleave(__ldg(reinterpret_cast<const uint4 *>(
                                     a.vin + (size_t)(c.r0 + c.tb + t) * K + g * 32 + wd * 8)));
                             }
@@ -283,12 +306,13 @@ __device__ __forceinline__ void dec_finish(float (&acc)[RU][DecTraits<MODE, L, R
                     acc[ru][b][t] += __shfl_xor_sync(0xffffffffu, acc[ru][b][t], off);
 #pragma unroll
     for (int ru = 0; ru < RU; ++ru) {
-        const int unit = c.unit0 + us + ru * Tr::UPW;
+        const int lr = us + ru * Tr::UPW;
+        const int unit = c.unit0 + lr;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const int r = c.r0 + c.tb + t;
             const int p = s_pairs[r];
-            if (unit < a.rows && (t % L) == ks) {
+            if (lr < c.cnt && (t % L) == ks) {
                 if (p < 0 || p >= a.P) {
                     set_error(a.err, MOE_DEVERR_BAD_METADATA);
                 } else if (MODE == kDecGateUp) {
@@ -307,37 +331,6 @@ __device__ __forceinline__ void dec_finish(float (&acc)[RU][DecTraits<MODE, L, R
         for (int b = 0; b < nmat; ++b)
 #pragma unroll
             for (int t = 0; t < kDecPass; ++t) acc[ru][b][t] = 0.f;
-}
-
-// Step 4, after a task's last pass: count its rows into their 8-row output
-// blocks; the warp that completes a block sums each token's k terms in order.
-// Every lane's y writes precede lane 0's fence and atomic (__syncwarp), and
-// the completing warp fences before reading the other warps' y rows.
-__device__ __forceinline__ void dec_combine(int n_lo, int n_hi, int A, const DecodeArgs &a, int lane) {
-    __syncwarp();
-    for (int nb = n_lo / 8; nb <= (n_hi - 1) / 8; ++nb) {
-        const int covered = min(n_hi, nb * 8 + 8) - max(n_lo, nb * 8);
-        unsigned old = 0;
-        if (lane == 0) {
-            __threadfence();
-            old = atomicAdd(a.counters + nb, (unsigned)covered);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old + covered == (unsigned)A * 8u) {
-            __threadfence();
-            for (int idx = lane; idx < a.T * 8; idx += 32) {
-                const int t = idx >> 3, n = nb * 8 + (idx & 7);
-                float accv = 0.f;
-                for (int jj = 0; jj < a.k; ++jj) {
-                    const int p = t * a.k + jj;
-                    accv = fmaf(__ldg(a.topk_w + p), __ldcg(a.y_out + (size_t)p * a.N + n), accv);
-                }
-                a.out[(size_t)t * a.N + n] = __float2half_rn(accv);
-            }
-            __syncwarp();
-            if (lane == 0) atomicExch(a.counters + nb, 0u);
-        }
-    }
 }
 
 // Cooperative copy of n activation rows (starting at src) into cache slots
@@ -360,18 +353,20 @@ __device__ __forceinline__ void dec_stage_rows(const __half *src, int n, int K, 
     }
 }
 
-template <int MODE, int L, int RU>
+template <int MODE, int L, int RU, int GT>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs a) {
     using Tr = DecTraits<MODE, L, RU>;
     constexpr int nmat = Tr::nmat;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int K = a.K, G = K / 32;
-    const DecLayout Ly = dec_layout(a.E, a.P, a.slots, K, a.wbytes);
+    const int G = GT ? GT : a.K / 32;
+    const int K = 32 * G;
+    const DecLayout Ly = dec_layout(a.E, a.P, a.nblk, a.slots, K, a.wbytes);
     const WarpGeom wg = warp_geom(Tr::RT, nmat, K);
     int *s_meta = reinterpret_cast<int *>(smem + Ly.meta);
     int *s_active = s_meta + 4;
     int *s_offs = s_active + a.E;
     int *s_pairs = s_offs + a.E + 1;
+    int *s_blk = reinterpret_cast<int *>(smem + Ly.blk);  // [nblk] counts, [nblk] done list, [1] n done
     uint8_t *xcb = smem + Ly.xc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *wb = smem + Ly.wbuf + (size_t)warp * a.wbytes;
@@ -381,10 +376,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         mbar_init(bar, 1);
         fence_mbar_init();
     }
+    for (int i = tid; i < 2 * a.nblk + 1; i += kDecThreads) s_blk[i] = 0;
     pdl_wait();
     pdl_trigger();
 
-    // ---- prologue: metadata (+ every x row in step 3), all loads first
+    // ---- prologue: metadata and activations, all loads first
     {
         const int nmeta = a.E + (a.E + 1) + a.P;  // active | offsets | pairs
         for (int base = 0; base < nmeta; base += 4 * kDecThreads) {
@@ -407,28 +403,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
             }
         }
         if (tid == 0) s_meta[0] = __ldg(a.num_active);
-        if (MODE == kDecGateUp) dec_stage_rows(a.vin, a.T, K, G, xcb, tid);
+        // step 3: every x row; step 4: every h row when the cache holds them
+        if (MODE == kDecGateUp || a.slots >= a.P) dec_stage_rows(a.vin, MODE == kDecGateUp ? a.T : a.P, K, G, xcb, tid);
     }
     __syncthreads();
+    const bool hc = MODE == kDecDown && a.slots >= a.P;
 
     int A = s_meta[0];
     A = A < 0 ? 0 : (A > a.E ? a.E : A);
     const int TPE = (a.rows + Tr::RT - 1) / Tr::RT;  // tasks per expert
-    const long long U = (long long)A * TPE;
-    const long long NW = (long long)gridDim.x * kDecWarps;
-    const long long gw = (long long)blockIdx.x * kDecWarps + warp;
-    const int t0 = (int)(U * gw / NW), t1 = (int)(U * (gw + 1) / NW);
+    const int U = A * TPE;
+    // tasks dealt round-robin: CTA first, then warp
+    const int ustride = gridDim.x * kDecWarps;
+    int u = blockIdx.x + gridDim.x * warp;
 
-    // task u's expert and segment; false (and flagged) if the metadata is bad
-    auto task = [&](int u, Cursor &c) -> bool {
-        const int ai = u / TPE;
+    // task u's expert and segment; false if the metadata is bad
+    auto task = [&](int uu, Cursor &c) -> bool {
+        const int ai = uu / TPE;
         c.e = s_active[ai];
         if (c.e < 0 || c.e >= a.E) return false;
         c.r0 = s_offs[c.e];
         const int r1 = s_offs[c.e + 1];
         if (c.r0 < 0 || r1 > a.P || r1 <= c.r0) return false;
         c.ne = r1 - c.r0;
-        c.unit0 = (u - ai * TPE) * Tr::RT;
+        c.unit0 = (uu - ai * TPE) * Tr::RT;
         c.cnt = min(Tr::RT, a.rows - c.unit0);
         c.tb = 0;
         return true;
@@ -455,36 +453,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         }
     };
 
-    // the first task of this warp goes out before anything else is waited for
-    int u = t0;
     Cursor cur;
-    while (u < t1 && !task(u, cur)) {
+    while (u < U && !task(u, cur)) {
         if (lane == 0) set_error(a.err, MOE_DEVERR_BAD_METADATA);
-        ++u;
+        u += ustride;
     }
-    if (u < t1) issue(cur);
+    if (u < U) issue(cur);
 
-    // ---- step 4: cache the h rows of every segment this CTA touches
-    int hbase = 0;
-    bool hcached = false;
-    if (MODE == kDecDown) {
-        const int c0 = (int)(U * blockIdx.x * kDecWarps / NW);
-        const int c1 = (int)(U * (blockIdx.x + 1) * kDecWarps / NW);
-        if (c1 > c0) {
-            const int e0 = s_active[c0 / TPE], e1 = s_active[(c1 - 1) / TPE];
-            if (e0 >= 0 && e0 < a.E && e1 >= 0 && e1 < a.E) {
-                const int R0 = s_offs[e0], R1 = s_offs[e1 + 1];
-                if (R0 >= 0 && R0 <= R1 && R1 <= a.P && R1 - R0 <= a.slots) {
-                    dec_stage_rows(a.vin + (size_t)R0 * K, R1 - R0, K, G, xcb, tid);
-                    hbase = R0;
-                    hcached = true;
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    float acc[RU][nmat][kDecPass];
+    float acc[Tr::RT > 0 ? RU : 1][nmat][kDecPass];
 #pragma unroll
     for (int ru = 0; ru < RU; ++ru)
 #pragma unroll
@@ -492,76 +468,124 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
 #pragma unroll
             for (int t = 0; t < kDecPass; ++t) acc[ru][b][t] = 0.f;
     uint32_t phase = 0;
-    while (u < t1) {
+    bool dead = false;
+    while (u < U) {
         if (!mbar_wait_bounded(bar, phase, nullptr)) {
             if (lane == 0) set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
             mbar_wait_bounded(bar, phase, nullptr);  // never leave with a copy in flight
-            return;
+            dead = true;
+            break;
         }
         phase ^= 1u;
-        const bool hc = hcached && cur.r0 >= hbase && cur.r0 + cur.ne - hbase <= a.slots;
         // segments longer than a pass (several tokens on one expert) take more passes
         for (cur.tb = 0; cur.tb < cur.ne; cur.tb += kDecPass) {
             const int nt = min(kDecPass, cur.ne - cur.tb);
             switch (nt) {
                 case 1:
-                    dec_compute<MODE, L, RU, 1>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_compute<MODE, L, RU, GT, 1>(wb, wg, acc, cur, s_pairs, xcb, hc, a, lane);
                     dec_finish<MODE, L, RU, 1>(acc, cur, s_pairs, a, lane);
                     break;
                 case 2:
-                    dec_compute<MODE, L, RU, 2>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_compute<MODE, L, RU, GT, 2>(wb, wg, acc, cur, s_pairs, xcb, hc, a, lane);
                     dec_finish<MODE, L, RU, 2>(acc, cur, s_pairs, a, lane);
                     break;
                 case 3:
-                    dec_compute<MODE, L, RU, 3>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_compute<MODE, L, RU, GT, 3>(wb, wg, acc, cur, s_pairs, xcb, hc, a, lane);
                     dec_finish<MODE, L, RU, 3>(acc, cur, s_pairs, a, lane);
                     break;
                 default:
-                    dec_compute<MODE, L, RU, 4>(wb, wg, acc, cur, s_pairs, xcb, hbase, hc, a, lane);
+                    dec_compute<MODE, L, RU, GT, 4>(wb, wg, acc, cur, s_pairs, xcb, hc, a, lane);
                     dec_finish<MODE, L, RU, 4>(acc, cur, s_pairs, a, lane);
                     break;
             }
         }
-        if (MODE == kDecDown) dec_combine(cur.unit0, cur.unit0 + cur.cnt, A, a, lane);
+        if (MODE == kDecDown && lane == 0) {
+            // count this task's rows into its 8-row output blocks (shared)
+            const int n_lo = cur.unit0, n_hi = cur.unit0 + cur.cnt;
+            for (int nb = n_lo / 8; nb <= (n_hi - 1) / 8; ++nb)
+                atomicAdd(&s_blk[nb], min(n_hi, nb * 8 + 8) - max(n_lo, nb * 8));
+        }
         __syncwarp();
-        // next valid task
-        for (++u; u < t1 && !task(u, cur); ++u)
+        // next valid task of this warp
+        for (u += ustride; u < U && !task(u, cur); u += ustride)
             if (lane == 0) set_error(a.err, MOE_DEVERR_BAD_METADATA);
-        if (u < t1) issue(cur);
+        if (u < U) issue(cur);
+    }
+
+    if (MODE == kDecDown) {
+        // Publish this CTA's row counts: the y rows of every warp precede the
+        // barrier, the barrier precedes each publishing thread's fence and
+        // atomic.  A thread whose atomic completes a block queues it.
+        __syncthreads();
+        int *s_done = s_blk + a.nblk, *s_ndone = s_blk + 2 * a.nblk;
+        for (int nb = tid; nb < a.nblk; nb += kDecThreads) {
+            const int cnt = s_blk[nb];
+            if (cnt == 0 || dead) continue;
+            __threadfence();
+            const unsigned old = atomicAdd(a.counters + nb, (unsigned)cnt);
+            if (old + cnt == (unsigned)A * 8u) {
+                __threadfence();
+                s_done[atomicAdd(s_ndone, 1)] = nb;
+            }
+        }
+        __syncthreads();
+        const int ndone = *s_ndone;
+        if (ndone > 0) __threadfence();
+        // each completed block: out[t][8 rows] = sum_j w[t][j] * y[t*k+j] in j order
+        for (int d = warp; d < ndone; d += kDecWarps) {
+            const int nb = s_done[d];
+            for (int idx = lane; idx < a.T * 8; idx += 32) {
+                const int t = idx >> 3, n = nb * 8 + (idx & 7);
+                float accv = 0.f;
+#pragma unroll 8
+                for (int jj = 0; jj < a.k; ++jj) {  // unrolled: the loads go out together
+                    const int p = t * a.k + jj;
+                    accv = fmaf(__ldg(a.topk_w + p), __ldcg(a.y_out + (size_t)p * a.N + n), accv);
+                }
+                a.out[(size_t)t * a.N + n] = __float2half_rn(accv);
+            }
+            __syncwarp();
+            if (lane == 0) atomicExch(a.counters + nb, 0u);
+        }
     }
 }
 
 // ---------------------------------------------------------------- launchers
-template <int MODE, int L, int RU>
+template <int MODE, int L, int RU, int GT>
 static cudaError_t launch_decode_t(DecodeArgs a, int num_sms, size_t smem_limit, cudaStream_t stream) {
     using Tr = DecTraits<MODE, L, RU>;
     a.wbytes = warp_geom(Tr::RT, Tr::nmat, a.K).bytes;
-    const size_t smem = dec_layout(a.E, a.P, a.slots, a.K, a.wbytes).total;
+    const size_t smem = dec_layout(a.E, a.P, a.nblk, a.slots, a.K, a.wbytes).total;
     if (smem > smem_limit) return cudaErrorInvalidConfiguration;
     static int configured[128];
-    cudaError_t e = ensure_smem(decode_kernel<MODE, L, RU>, configured, smem);
+    cudaError_t e = ensure_smem(decode_kernel<MODE, L, RU, GT>, configured, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_kernel<MODE, L, RU>, num_sms, kDecThreads, smem, stream, a);
+    return launch_pdl(decode_kernel<MODE, L, RU, GT>, num_sms, kDecThreads, smem, stream, a);
 }
 
 // Lanes per row unit: a power of two giving each lane about five groups.
 static int lanes_for(int G) { return G >= 40 ? 8 : (G >= 20 ? 4 : (G >= 10 ? 2 : 1)); }
 
-
-static int lanes_for(int G);
-
-// Largest per-warp buffer the decode kernels need for these sizes (step 3:
-// one task of 32/L row pairs; step 4: one task of 2*32/L rows).
+// Per-warp buffer of the decode kernels (step 3: a task of 32/L row pairs;
+// step 4: a task of 2*32/L rows).
 static uint32_t decode_wbytes(int H, int I, bool gate_up) {
     const int G = (gate_up ? H : I) / 32, L = lanes_for(G);
     return gate_up ? warp_geom(32 / L, 2, H).bytes : warp_geom(2 * (32 / L), 1, I).bytes;
 }
 
+// step 4 caches every h row when they fit next to its task buffers
+static int down_slots(int T, int E, int k, int H, int I, size_t smem_limit) {
+    const int P = T * k;
+    const uint32_t wb = decode_wbytes(H, I, false);
+    return dec_layout(E, P, H / 8, P, I, wb).total <= smem_limit ? P : 0;
+}
+
 bool decode_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int P = T * k;
     return T >= 1 && T <= kDecMaxT &&
-           dec_layout(E, P, T, H, decode_wbytes(H, I, true)).total <= smem_limit &&
-           dec_layout(E, P, 4 * T, I, decode_wbytes(H, I, false)).total <= smem_limit;
+           dec_layout(E, P, 0, T, H, decode_wbytes(H, I, true)).total <= smem_limit &&
+           dec_layout(E, P, H / 8, down_slots(T, E, k, H, I, smem_limit), I,
+                      decode_wbytes(H, I, false)).total <= smem_limit;
 }
 
 cudaError_t launch_gate_up_decode(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
@@ -576,11 +600,14 @@ cudaError_t launch_gate_up_decode(const __half *x, const uint32_t *q, const __ha
     a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
     a.h_out = h; a.err = err;
     a.slots = T;
-    switch (lanes_for(H / 32)) {
-        case 8: return launch_decode_t<kDecGateUp, 8, 1>(a, num_sms, smem_limit, stream);
-        case 4: return launch_decode_t<kDecGateUp, 4, 1>(a, num_sms, smem_limit, stream);
-        case 2: return launch_decode_t<kDecGateUp, 2, 1>(a, num_sms, smem_limit, stream);
-        default: return launch_decode_t<kDecGateUp, 1, 1>(a, num_sms, smem_limit, stream);
+    a.nblk = 0;
+    const int G = H / 32;
+    if (G == 80) return launch_decode_t<kDecGateUp, 8, 1, 80>(a, num_sms, smem_limit, stream);
+    switch (lanes_for(G)) {
+        case 8: return launch_decode_t<kDecGateUp, 8, 1, 0>(a, num_sms, smem_limit, stream);
+        case 4: return launch_decode_t<kDecGateUp, 4, 1, 0>(a, num_sms, smem_limit, stream);
+        case 2: return launch_decode_t<kDecGateUp, 2, 1, 0>(a, num_sms, smem_limit, stream);
+        default: return launch_decode_t<kDecGateUp, 1, 1, 0>(a, num_sms, smem_limit, stream);
     }
 }
 
@@ -595,12 +622,16 @@ cudaError_t launch_down_decode(const __half *h, const uint32_t *q, const __half 
     a.vin = h; a.T = T; a.k = k; a.P = T * k;
     a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
     a.y_out = y; a.topk_w = topk_w; a.out = out; a.counters = counters; a.err = err;
-    a.slots = 4 * T;  // h rows of a few segments; more fall back to direct reads
-    switch (lanes_for(I / 32)) {
-        case 8: return launch_decode_t<kDecDown, 8, 2>(a, num_sms, smem_limit, stream);
-        case 4: return launch_decode_t<kDecDown, 4, 2>(a, num_sms, smem_limit, stream);
-        case 2: return launch_decode_t<kDecDown, 2, 2>(a, num_sms, smem_limit, stream);
-        default: return launch_decode_t<kDecDown, 1, 2>(a, num_sms, smem_limit, stream);
+    a.slots = down_slots(T, E, k, H, I, smem_limit);
+    a.nblk = H / 8;
+    const int G = I / 32;
+    if (G == 20) return launch_decode_t<kDecDown, 4, 2, 20>(a, num_sms, smem_limit, stream);
+    if (G == 5) return launch_decode_t<kDecDown, 1, 2, 5>(a, num_sms, smem_limit, stream);
+    switch (lanes_for(G)) {
+        case 8: return launch_decode_t<kDecDown, 8, 2, 0>(a, num_sms, smem_limit, stream);
+        case 4: return launch_decode_t<kDecDown, 4, 2, 0>(a, num_sms, smem_limit, stream);
+        case 2: return launch_decode_t<kDecDown, 2, 2, 0>(a, num_sms, smem_limit, stream);
+        default: return launch_decode_t<kDecDown, 1, 2, 0>(a, num_sms, smem_limit, stream);
     }
 }
 
