@@ -351,7 +351,7 @@ def main():
             "layer_us": {"median": float(np.median(layer_ms) * 1e3),
                          "p10": float(np.percentile(layer_ms, 10) * 1e3),
                          "p90": float(np.percentile(layer_ms, 90) * 1e3)},
-            "roofline": {"kernel": "moe_w4a16_gate_up_silu (stream_kernel<gate_up>)",
+            "roofline": {"kernel": "moe_w4a16_gate_up_silu (decode_kernel<gate_up>)" if T <= 8 else "moe_w4a16_gate_up_silu (stream_kernel<gate_up>)",
                          "bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s",
                          "frac": gu_gbs / peak, "peak_source": peak_kind,
                          "gate_up_us_median": float(np.median(gu_ms) * 1e3),

@@ -182,6 +182,36 @@ int moe_w4a16_down_combine(const uint16_t *h,
                            uint16_t *out, void *workspace, size_t ws_bytes,
                            void *stream);
 
+/* The whole layer in one call: steps 1-4 above, in order, with the same
+ * arithmetic and results (routing ids and weights bit-identical to
+ * moe_topk_route; h and out as steps 3 and 4).  The method is the layer of
+ * the overview (route with renormalised top-k softmax, group the pairs into
+ * active-expert segments, gate/up + SiLU, down, weighted combine); the
+ * single entry point is this library's own.
+ *   logits f32 [T][E], x f16 [T][H]   (read)
+ *   w13_*, w2_*                        packed weights as in steps 3 and 4
+ *   topk_ids i32 [T][k], topk_w f32 [T][k]  (written) step 1 outputs
+ *   out    f16 [T][H]                  (written)
+ *   workspace: at least moe_layer_workspace_bytes(T, E, k, H, I) bytes, with
+ *   the rules of the workspace paragraph above; it holds the grouping, h
+ *   and the per-pair projections.
+ * For decode batches (T <= 8, T*k <= 256) whose buffers fit one SM's shared
+ * memory, the layer runs as one cooperative kernel (one CTA per SM, all
+ * resident): every CTA routes and groups the tokens itself, and the CTAs
+ * wait on each other only where a step needs another CTA's results (h of
+ * an expert before its down rows, all of a block's rows before its
+ * combine), with bounded waits that report MOE_DEVERR_WAIT_TIMEOUT.  Other
+ * sizes run the four steps as separate launches.  `out` must not alias any
+ * input. */
+size_t moe_layer_workspace_bytes(int T, int E, int k, int H, int I);
+
+int moe_w4a16_moe_layer(const float *logits, const uint16_t *x,
+                        const uint32_t *w13_q, const uint16_t *w13_s, const uint32_t *w13_z,
+                        const uint32_t *w2_q, const uint16_t *w2_s, const uint32_t *w2_z,
+                        int group_size, int T, int E, int k, int H, int I,
+                        int32_t *topk_ids, float *topk_w, uint16_t *out,
+                        void *workspace, size_t ws_bytes, void *stream);
+
 /* Step 4 for callers that cannot allocate device memory.  The paper has no
  * counterpart: this is a convenience of this library.  Some callers are not
  * allowed to call cudaMalloc -- an engine that plans all device memory

@@ -32,7 +32,7 @@ MOE_DEVERR_BAD_METADATA = 0x4
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes",
             "moe_get_device_error", "moe_topk_route", "moe_align_offsets", "moe_topk_route_align",
             "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine",
-            "moe_w4a16_down_combine_noalloc")
+            "moe_w4a16_down_combine_noalloc", "moe_layer_workspace_bytes", "moe_w4a16_moe_layer")
 
 _lock = threading.Lock()
 _lib = None
@@ -80,6 +80,11 @@ def load_library(path: str = LIB_PATH):
         lib.moe_w4a16_down_combine_noalloc.restype = _I
         lib.moe_w4a16_down_combine_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                        _I, _I, _I, _I, _I, _P, _P]
+        lib.moe_layer_workspace_bytes.restype = _SZ
+        lib.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+        lib.moe_w4a16_moe_layer.restype = _I
+        lib.moe_w4a16_moe_layer.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                            _P, _P, _P, _P, _SZ, _P]
         _lib = lib
         return lib
 
@@ -118,6 +123,20 @@ def new_workspace(T: int, E: int, k: int, H: int, I: int, device="cuda"):
     n = workspace_bytes(T, E, k, H, I)
     if n == 0:
         raise MoEError("moe_workspace_bytes", MOE_ERR_INVALID_ARG, "sizes rejected")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def layer_workspace_bytes(T: int, E: int, k: int, H: int, I: int) -> int:
+    return int(load_library().moe_layer_workspace_bytes(T, E, k, H, I))
+
+
+def new_layer_workspace(T: int, E: int, k: int, H: int, I: int, device="cuda"):
+    """A zero-filled workspace for moe_w4a16_moe_layer (also large enough for
+    every step call of the same shape)."""
+    import torch
+    n = layer_workspace_bytes(T, E, k, H, I)
+    if n == 0:
+        raise MoEError("moe_layer_workspace_bytes", MOE_ERR_INVALID_ARG, "sizes rejected")
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
@@ -250,6 +269,32 @@ def moe_w4a16_down_combine_noalloc(h, w2, meta, topk_w, out=None, stream=None, g
     return out
 
 
+def moe_w4a16_moe_layer(logits, x, w13, w2, k: int, workspace, topk_ids=None, topk_w=None,
+                        out=None, stream=None, group_size=32):
+    """The whole layer in one C call; returns (out, topk_ids, topk_w)."""
+    import torch
+    T, E = logits.shape
+    H = x.shape[1]
+    I = w2[0].shape[2] * 8
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float16, device=logits.device)
+    q13, s13, z13 = w13
+    q2, s2, z2 = w2
+    st = load_library().moe_w4a16_moe_layer(
+        _dev(logits, torch.float32, "logits"), _dev(x, torch.float16, "x"),
+        _dev(q13, torch.int32, "w13_q"), _dev(s13, torch.float16, "w13_s"), _dev(z13, torch.int32, "w13_z"),
+        _dev(q2, torch.int32, "w2_q"), _dev(s2, torch.float16, "w2_s"), _dev(z2, torch.int32, "w2_z"),
+        group_size, T, E, k, H, I, _dev(topk_ids, torch.int32, "topk_ids"),
+        _dev(topk_w, torch.float32, "topk_w"), _dev(out, torch.float16, "out"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check("moe_w4a16_moe_layer", st)
+    return out, topk_ids, topk_w
+
+
 def to_device_weights(w, device="cuda"):
     """(qweight, scales, qzeros) numpy arrays -> CUDA tensors (u32 viewed as int32)."""
     import numpy as np
@@ -279,7 +324,8 @@ class MoELayer:
                      torch.empty(1, dtype=torch.int32, device=dev))
         self.h = torch.empty((P, self.I), dtype=torch.float16, device=dev)
         self.out = torch.empty((T, self.H), dtype=torch.float16, device=dev)
-        self.workspace = new_workspace(T, E, k, self.H, self.I, device=dev)
+        # sized for the one-call layer too (a superset of the step calls' needs)
+        self.workspace = new_layer_workspace(T, E, k, self.H, self.I, device=dev)
 
     def forward(self, logits, x, stream=None):
         moe_topk_route(logits, self.k, self.topk_ids, self.topk_w, stream=stream)
@@ -290,10 +336,17 @@ class MoELayer:
                                out=self.out, stream=stream)
         return self.out
 
+    def forward_layer(self, logits, x, stream=None):
+        """The same layer through the one-call entry point."""
+        moe_w4a16_moe_layer(logits, x, self.w13, self.w2, self.k, self.workspace,
+                            topk_ids=self.topk_ids, topk_w=self.topk_w, out=self.out, stream=stream)
+        return self.out
+
     def bind(self, logits, x, stream=None):
         """Pre-marshals the four calls for fixed input buffers; returns four
         zero-argument callables (route, align, gate_up, down) that each make
-        one C call, and sets self.route_align_call (steps 1-2 in one call).
+        one C call, and sets self.route_align_call (steps 1-2 in one call) and
+        self.layer_call (the whole layer through moe_w4a16_moe_layer).
         Used where host overhead must stay off the timeline."""
         import torch
         lib = load_library()
@@ -321,6 +374,9 @@ class MoELayer:
         a_ra = (logits.data_ptr(), T, E, k, self.topk_ids.data_ptr(), self.topk_w.data_ptr(),
                 offs, sp, act, na, ws, wsb, st)
         self.route_align_call = call(lib.moe_topk_route_align, "moe_topk_route_align", a_ra)
+        a_layer = (logits.data_ptr(), x.data_ptr(), q13, s13, z13, q2, s2, z2, 32, T, E, k, H, I,
+                   self.topk_ids.data_ptr(), self.topk_w.data_ptr(), self.out.data_ptr(), ws, wsb, st)
+        self.layer_call = call(lib.moe_w4a16_moe_layer, "moe_w4a16_moe_layer", a_layer)
         return (call(lib.moe_topk_route, "moe_topk_route", a_route),
                 call(lib.moe_align_offsets, "moe_align_offsets", a_align),
                 call(lib.moe_w4a16_gate_up_silu, "moe_w4a16_gate_up_silu", a_gu),

@@ -34,6 +34,13 @@ cudaError_t launch_down_decode(const __half *, const uint32_t *, const __half *,
                                const float *, int, int, int, int, int, __half *, float *, uint32_t *,
                                uint32_t *, int, size_t, cudaStream_t);
 
+bool layer_fusable(int, int, int, int, int, int, size_t);
+cudaError_t launch_decode_layer(const float *, const __half *, const uint32_t *, const __half *,
+                                const uint32_t *, const uint32_t *, const __half *, const uint32_t *,
+                                int, int, int, int, int, int32_t *, float *, __half *, __half *,
+                                float *, uint32_t *, uint32_t *, uint32_t *, uint32_t *, int, size_t,
+                                cudaStream_t);
+
 namespace {
 
 constexpr int kMaxE = 1024;
@@ -258,4 +265,81 @@ MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, c
                            reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms,
                            di.smem_optin, static_cast<cudaStream_t>(stream));
     return cuda_status(e);
+}
+
+namespace moe {
+namespace {
+
+// The layer call's workspace: the workspace of steps 3 and 4 (control
+// words, block counters, per-pair y), then the grouping outputs, h, and the
+// per-expert and exit counters of the one-launch decode layer.
+struct LayerWorkspace {
+    size_t offsets, sorted, active, num_active, h, done, exitctr, total;
+};
+
+LayerWorkspace layer_workspace(int T, int E, int k, int H, int I) {
+    LayerWorkspace L;
+    const size_t P = (size_t)T * k;
+    L.offsets = workspace_layout(T, k, H).total;
+    L.sorted = L.offsets + align_up((size_t)(E + 1) * 4, 256);
+    L.active = L.sorted + align_up(P * 4, 256);
+    L.num_active = L.active + align_up((size_t)E * 4, 256);
+    L.h = L.num_active + 256;
+    L.done = L.h + align_up(P * I * 2, 256);
+    L.exitctr = L.done + align_up(P * 4, 256);
+    L.total = L.exitctr + 256;
+    return L;
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_EXPORT size_t moe_layer_workspace_bytes(int T, int E, int k, int H, int I) {
+    if (check_sizes(T, E, k, H, I) != MOE_OK) return 0;
+    return layer_workspace(T, E, k, H, I).total;
+}
+
+MOE_EXPORT int moe_w4a16_moe_layer(const float *logits, const uint16_t *x, const uint32_t *w13_q,
+                                   const uint16_t *w13_s, const uint32_t *w13_z, const uint32_t *w2_q,
+                                   const uint16_t *w2_s, const uint32_t *w2_z, int group_size, int T,
+                                   int E, int k, int H, int I, int32_t *topk_ids, float *topk_w,
+                                   uint16_t *out, void *workspace, size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if ((st = check_group(group_size)) != MOE_OK) return st;
+    if (!all_aligned(w13_q, w13_s, w13_z, w2_q, w2_s, w2_z)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !all_aligned(logits, x, topk_ids, topk_w, out)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_layer_workspace_bytes(T, E, k, H, I))
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const WorkspaceLayout W = workspace_layout(T, k, H);
+    const LayerWorkspace L = layer_workspace(T, E, k, H, I);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
+    if (layer_fusable(T, E, k, H, I, di.sms, di.smem_optin))
+        return cuda_status(launch_decode_layer(
+            logits, reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s),
+            w13_z, w2_q, reinterpret_cast<const __half *>(w2_s), w2_z, T, E, k, H, I, topk_ids, topk_w,
+            reinterpret_cast<__half *>(out), reinterpret_cast<__half *>(ws + L.h),
+            reinterpret_cast<float *>(ws + W.y), reinterpret_cast<uint32_t *>(ws + W.counters),
+            reinterpret_cast<uint32_t *>(ws + L.done), reinterpret_cast<uint32_t *>(ws + L.exitctr), err,
+            di.sms, di.smem_optin, s));
+    // the four steps as separate launches
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    int32_t *active = reinterpret_cast<int32_t *>(ws + L.active);
+    int32_t *num_active = reinterpret_cast<int32_t *>(ws + L.num_active);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    if ((st = moe_topk_route_align(logits, T, E, k, topk_ids, topk_w, offsets, sorted, active, num_active,
+                                   workspace, ws_bytes, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_w4a16_gate_up_silu(x, w13_q, w13_s, w13_z, group_size, offsets, sorted, active,
+                                     num_active, T, E, k, H, I, h, workspace, ws_bytes, stream)) != MOE_OK)
+        return st;
+    return moe_w4a16_down_combine(h, w2_q, w2_s, w2_z, group_size, offsets, sorted, active, num_active,
+                                  topk_w, T, E, k, H, I, out, workspace, ws_bytes, stream);
 }

@@ -1,0 +1,83 @@
+// decode_layer.cu -- planning and dispatch of the one-launch decode layer
+// (kernel and method: decode_layer.cuh).
+#include "decode_layer.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+// Lanes per gate/up row pair and per down row: about five groups per lane,
+// task buffers of a few kilobytes.
+int layer_l1(int G1) { return G1 >= 40 ? 16 : (G1 >= 10 ? 4 : 1); }
+int layer_l2(int G2) { return G2 >= 10 ? 4 : 1; }
+
+LayerPlan layer_plan(int T, int E, int k, int H, int I, int num_sms, size_t smem_limit) {
+    LayerPlan pl{};
+    const int P = T * k;
+    if (T < 1 || T > kLayerMaxT || P > kLayerMaxPairs || E > 32 * kLayerRoutePer || num_sms < 1) return pl;
+    const int G1 = H / 32, G2 = I / 32;
+    pl.L1 = layer_l1(G1);
+    pl.L2 = layer_l2(G2);
+    const int RT1 = 32 / pl.L1, RT2 = 2 * (32 / pl.L2);
+    const uint32_t b1 = warp_geom(RT1, 2, H).bytes, b2 = warp_geom(RT2, 1, I).bytes;
+    pl.slot_bytes = b1 > b2 ? b1 : b2;
+    // h rows one CTA's down share can read: its experts (at most the tasks
+    // over the tasks per expert, plus one) times T rows each
+    const int TPE2 = (H + RT2 - 1) / RT2;
+    const long long Amax = P < E ? P : E;
+    const long long per_cta = (Amax * TPE2 + num_sms - 1) / num_sms;
+    const long long experts = (per_cta + TPE2 - 1) / TPE2 + 1;
+    long long hr = experts * T;
+    pl.hrows = (int)(hr < P ? hr : P);
+    for (int nw = kLayerMaxWarps; nw >= kLayerMinWarps; --nw) {
+        if (nw <= T) break;  // warps beyond the T routing warps stage x
+        const size_t smem = layer_layout(T, H, I, P, pl.hrows, nw, pl.slot_bytes).total;
+        if (smem <= smem_limit) {
+            pl.nw = nw;
+            pl.smem = smem;
+            pl.ok = true;
+            break;
+        }
+    }
+    return pl;
+}
+
+}  // namespace
+
+bool layer_fusable(int T, int E, int k, int H, int I, int num_sms, size_t smem_limit) {
+    return layer_plan(T, E, k, H, I, num_sms, smem_limit).ok;
+}
+
+cudaError_t launch_decode_layer(const float *logits, const __half *x, const uint32_t *q13, const __half *s13,
+                                const uint32_t *z13, const uint32_t *q2, const __half *s2,
+                                const uint32_t *z2, int T, int E, int k, int H, int I, int32_t *topk_ids,
+                                float *topk_w, __half *out, __half *h, float *y, uint32_t *blkctr,
+                                uint32_t *done, uint32_t *exitctr, uint32_t *err, int num_sms,
+                                size_t smem_limit, cudaStream_t stream) {
+    const LayerPlan pl = layer_plan(T, E, k, H, I, num_sms, smem_limit);
+    if (!pl.ok) return cudaErrorInvalidConfiguration;
+    LayerArgs a{};
+    a.logits = logits; a.x = x;
+    a.q13 = q13; a.s13 = s13; a.z13 = z13; a.q2 = q2; a.s2 = s2; a.z2 = z2;
+    a.T = T; a.E = E; a.k = k; a.H = H; a.I = I; a.P = T * k;
+    a.topk_ids = topk_ids; a.topk_w = topk_w; a.out = out;
+    a.h = h; a.y = y; a.blkctr = blkctr; a.done = done; a.exitctr = exitctr; a.err = err;
+    a.nw = pl.nw; a.hrows = pl.hrows; a.slot_bytes = pl.slot_bytes;
+    const int G1 = H / 32, G2 = I / 32;
+    // the geometries the layer is specified on get compile-time group counts
+    if (G1 == 80 && pl.L1 == 16 && G2 == 20 && pl.L2 == 4)
+        return launch_layer_t<16, 80, 4, 20>(a, pl, num_sms, stream);
+    if (G1 == 80 && pl.L1 == 16 && G2 == 5 && pl.L2 == 1)
+        return launch_layer_t<16, 80, 1, 5>(a, pl, num_sms, stream);
+    switch (pl.L1 * 8 + pl.L2) {
+        case 16 * 8 + 4: return launch_layer_t<16, 0, 4, 0>(a, pl, num_sms, stream);
+        case 16 * 8 + 1: return launch_layer_t<16, 0, 1, 0>(a, pl, num_sms, stream);
+        case 4 * 8 + 4: return launch_layer_t<4, 0, 4, 0>(a, pl, num_sms, stream);
+        case 4 * 8 + 1: return launch_layer_t<4, 0, 1, 0>(a, pl, num_sms, stream);
+        case 1 * 8 + 4: return launch_layer_t<1, 0, 4, 0>(a, pl, num_sms, stream);
+        default: return launch_layer_t<1, 0, 1, 0>(a, pl, num_sms, stream);
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,10 @@
+// decode_layer_spec.cu -- instantiations of the one-launch decode layer kernel
+// (decode_layer.cuh), compiled apart from the others to keep builds parallel.
+#include "decode_layer.cuh"
+
+namespace moe {
+
+template cudaError_t launch_layer_t<16, 80, 4, 20>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
+template cudaError_t launch_layer_t<16, 80, 1, 5>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
+
+}  // namespace moe

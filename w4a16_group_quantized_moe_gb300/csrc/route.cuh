@@ -18,11 +18,12 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 }
 
 // Routes one token with one warp.  PER = logits held per lane (E <= 32*PER).
-// Writes ids and weights of token t; also ids into s_ids[t*k + j] if given.
+// Writes ids and weights of token t to every destination given (non-null):
+// topk_ids / topk_w at [t*k + j], and s_ids / s_w at [t*k + j].
 template <int PER>
 __device__ __forceinline__ void route_token(const float *__restrict__ row, int E, int k, int t,
                                             int32_t *__restrict__ topk_ids, float *__restrict__ topk_w,
-                                            int *s_ids) {
+                                            int *s_ids, float *s_w = nullptr) {
     const int lane = threadIdx.x & 31;
     uint32_t key[PER];  // 0 = no candidate
 #pragma unroll
@@ -69,9 +70,11 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     if (lane < k) {
-        topk_ids[(size_t)t * k + lane] = my_id;
-        topk_w[(size_t)t * k + lane] = ex / sum;
+        const float w = ex / sum;
+        if (topk_ids) topk_ids[(size_t)t * k + lane] = my_id;
+        if (topk_w) topk_w[(size_t)t * k + lane] = w;
         if (s_ids) s_ids[t * k + lane] = my_id;
+        if (s_w) s_w[t * k + lane] = w;
     }
 }
 
