@@ -1,19 +1,18 @@
 """Benchmark of the W4A16 group-32 MoE layer (libmoe_w4a16) on GB300.
 
-One step = the whole layer (route, align, gate_up+SiLU, down+combine: four C
-calls on one stream) over one batch of synthetic inputs already resident in
-HBM.  Default workload: Qwen4Exp-geometry decode, 1 token (hidden 2560,
+One step = the whole layer (route, group, gate_up+SiLU, down+combine) over
+one batch of synthetic inputs already resident in HBM, through the one-call
+entry point moe_w4a16_moe_layer (one cooperative launch for decode batches).
+Default workload: Qwen4Exp-geometry decode, 1 token (hidden 2560,
 intermediate 640, 512 experts, top-10, W4A16 g32).
 
-Timing: W untimed warm-up steps, then K timed steps.  Before every step L2
-is flushed by reading a 1 GiB buffer (outside the timed interval; a read
-leaves clean lines behind, so the step does not pay for write-backs of the
-flush itself) and the
-router logits rotate over 32 pre-generated sets so the active experts change
-from step to step.  Each step is bracketed by CUDA events on the launching
-stream, with events around the gate/up kernel for the roofline line.  The
-flush kernel also keeps the GPU busy while the host enqueues the step, so
-host launch overhead does not show up inside the events.
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
+events on the launching stream.  Inputs larger than L2: the layer's weights
+exist in NL distinct copies used in turn (a stack of MoE layers), so every
+step reads its active weights from HBM; the router logits rotate over 32
+pre-generated sets so the active experts change from step to step.  Also
+reported: the same step with L2 flushed (a 1 GiB read) before every step,
+which also evicts the kernel's code, and the four step calls.
 
 Multi-GPU: the layer has no cross-token exchange, so N GPUs run N independent
 replicas (weak scaling); value = all ranks' tokens / max-over-ranks time.
@@ -205,6 +204,31 @@ def run_reference(args, wl):
     print(json.dumps(line))
 
 
+def source_digest() -> str:
+    """Digest of the CUDA sources (to tell whether stored ncu counters still
+    describe the kernels that run)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "w4a16_group_quantized_moe_gb300", "csrc", "*.cu*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes per launch of the layer kernel from the committed ncu
+    summary, or None when it was taken on other sources or another workload."""
+    p = os.path.join(ROOT, "profiles", "decode_layer_traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("sources") != source_digest():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
 def main():
     args = parse()
     from w4a16_group_quantized_moe_gb300 import inputs
@@ -230,68 +254,91 @@ def main():
     w13, w2 = inputs.make_weights(E, H, I, wl.seed)
     dw13, dw2 = moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev)
     del w13, w2
-    layer = moe.MoELayer(dw13, dw2, T, k, device=dev)
+    # NL distinct copies of the layer's weights (a stack of MoE layers): step s
+    # uses copy s % NL, so between two uses of a copy the other NL-1 copies'
+    # active weights stream through L2 -- more than twice its 126 MB at every
+    # workload here -- and each step reads its weights from HBM.
+    b = inputs.bytes_per_expert(H, I)
+    per_step = min(E, T * k) * (b["w13"] + b["w2"])
+    NL = max(4, min(16, int(np.ceil(2 * 126e6 / max(per_step, 1))) + 1))
+    layers = [moe.MoELayer(dw13, dw2, T, k, device=dev)]
+    for _ in range(NL - 1):
+        c13 = tuple(t.clone() for t in dw13)
+        c2 = tuple(t.clone() for t in dw2)
+        layers.append(moe.MoELayer(c13, c2, T, k, device=dev))
     sets = []
-    for s in range(args.sets):
-        lg, xx = inputs.make_activations(T, H, E, wl.seed + 1000 + s, wl.hot_experts, wl.hot_bias)
+    for si in range(args.sets):
+        lg, xx = inputs.make_activations(T, H, E, wl.seed + 1000 + si, wl.hot_experts, wl.hot_bias)
         sets.append((torch.from_numpy(lg).to(dev), torch.from_numpy(xx).to(dev)))
     logits_buf = torch.empty((T, E), dtype=torch.float32, device=dev)
     x_buf = torch.empty((T, H), dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
-    route, align, gate_up, down = layer.bind(logits_buf, x_buf, stream)
-    flush = torch.ones((args.flush_mb << 20) // 4, dtype=torch.int32, device=dev)
-    flush_out = torch.empty((), dtype=torch.int64, device=dev)
+    steps4 = [ly.bind(logits_buf, x_buf, stream) for ly in layers]
+    calls = [ly.layer_call for ly in layers]
+    flush = torch.zeros((args.flush_mb << 20) // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
-    def flush_l2():
-        torch.sum(flush, dim=0, dtype=torch.int64, out=flush_out)
+    def flush_l2():  # a read of 1 GiB: evicts every line of L2 (data and code)
+        torch.sum(flush, dim=0, out=flush_out)
 
     # active-expert count of every logits set (for the algorithmic bytes)
     A_of = []
+    r0, a0, _, _ = steps4[0]
     for lg, xx in sets:
         logits_buf.copy_(lg)
-        x_buf.copy_(xx)
-        route(); align()
-        A_of.append(int(layer.meta[3].item()))
+        r0(); a0()
+        A_of.append(int(layers[0].meta[3].item()))
 
-    def step(s, ev=None):
+    def stage(s):
         lg, xx = sets[s % len(sets)]
         logits_buf.copy_(lg, non_blocking=True)
         x_buf.copy_(xx, non_blocking=True)
-        flush_l2()
-        if ev is not None:
-            ev[0].record(stream)
-        route(); align()
-        if ev is not None:
-            ev[1].record(stream)
-        gate_up()
-        if ev is not None:
-            ev[2].record(stream)
-        down()
-        if ev is not None:
-            ev[3].record(stream)
 
-    for s in range(args.warmup):
-        step(s)
-    torch.cuda.synchronize()
-    if moe.moe_get_device_error(layer.workspace):
-        raise RuntimeError("device error during warm-up")
+    def timed(n, first, fn, flush_each=False):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for j in range(n):
+            s = first + j
+            stage(s)
+            if flush_each:
+                flush_l2()
+            else:
+                # keep the GPU busy (~100 us) while the host enqueues the step, so
+                # host launch gaps never fall inside the events
+                torch.cuda._sleep(200000)
+            ev[j][0].record(stream)
+            fn(s)
+            ev[j][1].record(stream)
+        torch.cuda.synchronize()
+        return np.array([e[0].elapsed_time(e[1]) for e in ev])
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    one_call = lambda s: calls[s % NL]()
+
+    def four_calls(s):
+        r, a_, g, d = steps4[s % NL]
+        r(); a_(); g(); d()
+
+    timed(args.warmup, 0, one_call)
+    timed(min(args.warmup, 50), 0, four_calls)
+    for ly in layers:
+        if moe.moe_get_device_error(ly.workspace):
+            raise RuntimeError("device error during warm-up")
+
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        for s in range(args.steps):
-            step(args.warmup + s, evs[s])
-        torch.cuda.synchronize()
+        layer_ms = timed(args.steps, args.warmup, one_call)
     if world > 1:
         torch.distributed.barrier()
-    layer_ms = np.array([e[0].elapsed_time(e[3]) for e in evs])
-    gu_ms = np.array([e[1].elapsed_time(e[2]) for e in evs])
     A_steps = np.array([A_of[(args.warmup + s) % len(sets)] for s in range(args.steps)])
-    flag = moe.moe_get_device_error(layer.workspace)
-    if flag:
-        raise RuntimeError(f"device error word 0x{flag:x} during timed steps")
+    for ly in layers:
+        flag = moe.moe_get_device_error(ly.workspace)
+        if flag:
+            raise RuntimeError(f"device error word 0x{flag:x} during timed steps")
+    # secondary figures: the four step calls, and one call with L2 flushed
+    n2 = min(args.steps, 2000)
+    four_ms = timed(n2, 0, four_calls)
+    flushed_ms = timed(n2, 0, one_call, flush_each=True)
 
     tot_ms = float(layer_ms.sum())
     if world > 1:
@@ -300,13 +347,12 @@ def main():
         tot_ms = float(t.item())
     value = world * T * args.steps / (tot_ms / 1e3)
 
-    lb, gb = zip(*(active_bytes(int(a), T, k, H, I) for a in A_steps))
-    layer_gbs = float(np.sum(lb) / (layer_ms.sum() / 1e3) / 1e9)
-    gu_gbs = float(np.sum(gb) / (gu_ms.sum() / 1e3) / 1e9)
+    lb = np.array([active_bytes(int(a), T, k, H, I)[0] for a in A_steps])
+    layer_gbs = float(lb.sum() / (layer_ms.sum() / 1e3) / 1e9)
     peak, peak_kind, _ = peaks()
 
     # end to end through the C ABI with host buffers: H2D of the step's
-    # inputs from pinned memory, the four calls, D2H of the output
+    # inputs from pinned memory, the layer call, D2H of the output
     h_logits = [lg.cpu().pin_memory() for lg, _ in sets]
     h_x = [xx.cpu().pin_memory() for _, xx in sets]
     h_out = torch.empty((T, H), dtype=torch.float16).pin_memory()
@@ -314,12 +360,11 @@ def main():
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
     for s in range(e2e_steps):
         i = s % len(sets)
-        flush_l2()
         e2e_ev[s][0].record(stream)
         logits_buf.copy_(h_logits[i], non_blocking=True)
         x_buf.copy_(h_x[i], non_blocking=True)
-        route(); align(); gate_up(); down()
-        h_out.copy_(layer.out, non_blocking=True)
+        calls[s % NL]()
+        h_out.copy_(layers[s % NL].out, non_blocking=True)
         e2e_ev[s][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev)
@@ -337,6 +382,11 @@ def main():
                          f"{el:.1f} s, single-threaded fp64 C oracle"}
 
     if rank == 0:
+        fused = T <= 8
+        kernel = ("decode_layer_kernel (moe_w4a16_moe_layer, one cooperative launch)" if fused
+                  else "moe_w4a16_moe_layer (route_align, gate_up, down launches)")
+        traffic = stored_traffic(wl.name) if fused else None
+        med = lambda a: float(np.median(a) * 1e3)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
@@ -344,23 +394,26 @@ def main():
             "dtype": "f16", "data": "synthetic",
             "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
                        "group_size": 32, "parallelism": f"replicas x{world}",
-                       "l2": f"flushed before every timed step ({args.flush_mb} MiB read); "
-                             f"router logits rotated over {args.sets} sets",
+                       "l2": f"inputs larger than L2: {NL} distinct copies of the layer's weights "
+                             f"({NL * inputs.bytes_per_expert(H, I)['w13'] * E / 1e9 + NL * inputs.bytes_per_expert(H, I)['w2'] * E / 1e9:.1f} GB) "
+                             f"used in turn, so the {NL - 1} steps between two uses of a copy "
+                             f"stream >= {(NL - 1) * per_step / 1e6:.0f} MB of other weights through "
+                             f"the 126 MB L2; router logits rotate over {args.sets} sets",
                        "mean_active_experts": float(A_steps.mean())},
             "layer_hbm_gbs": layer_gbs,
-            "layer_us": {"median": float(np.median(layer_ms) * 1e3),
-                         "p10": float(np.percentile(layer_ms, 10) * 1e3),
+            "layer_us": {"median": med(layer_ms), "p10": float(np.percentile(layer_ms, 10) * 1e3),
                          "p90": float(np.percentile(layer_ms, 90) * 1e3)},
-            "roofline": {"kernel": "moe_w4a16_gate_up_silu (decode_kernel<gate_up>)" if T <= 8 else "moe_w4a16_gate_up_silu (stream_kernel<gate_up>)",
-                         "bound": "hbm", "achieved": gu_gbs, "peak": peak, "unit": "GB/s",
-                         "frac": gu_gbs / peak, "peak_source": peak_kind,
-                         "gate_up_us_median": float(np.median(gu_ms) * 1e3),
-                         "traffic": None},
+            "layer_us_l2_flushed_each_step": med(flushed_ms),
+            "layer_us_four_step_calls": med(four_ms),
+            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": layer_gbs, "peak": peak,
+                         "unit": "GB/s", "frac": layer_gbs / peak,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                         "traffic": traffic},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,
                     "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
-            "gpu_launches": (4 + (T > 8)) * args.steps,
+            "gpu_launches": (1 if fused else 3) * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line))

@@ -189,12 +189,20 @@ __device__ inline ZeroPoint make_zero_point(uint32_t z) {
     return zp;
 }
 
+// (a & mask) | 0x64006400 as one three-input logic instruction.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or_6400(uint32_t a) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "n"(MASK), "n"(0x64006400u));
+    return r;
+}
+
 __device__ inline void dequant_word(uint32_t w, const ZeroPoint &zp, __half2 *d) {
-    const uint32_t lo = (w & 0x000F000Fu) | 0x64006400u;
-    const uint32_t hi = (w & 0x00F000F0u) | 0x64006400u;
+    const uint32_t lo = and_or_6400<0x000F000Fu>(w);
+    const uint32_t hi = and_or_6400<0x00F000F0u>(w);
     const uint32_t w8 = w >> 8;
-    const uint32_t lo2 = (w8 & 0x000F000Fu) | 0x64006400u;
-    const uint32_t hi2 = (w8 & 0x00F000F0u) | 0x64006400u;
+    const uint32_t lo2 = and_or_6400<0x000F000Fu>(w8);
+    const uint32_t hi2 = and_or_6400<0x00F000F0u>(w8);
     const __half2 sixteenth = __float2half2_rn(0.0625f);
     d[0] = __hsub2(*reinterpret_cast<const __half2 *>(&lo), zp.z1024);
     d[1] = __hfma2(*reinterpret_cast<const __half2 *>(&hi), sixteenth, zp.neg_z64);

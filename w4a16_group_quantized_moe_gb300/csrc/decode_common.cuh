@@ -99,7 +99,8 @@ struct Cursor {
 // The kGPI groups of a step are worked on together, each product sum in up
 // to four independent fp16 chains.
 //
-// Activation rows: step 3 reads token p / k of pair p from cache slot p / k;
+// Activation rows: step 3 reads token p / k of pair p from cache slot p / k
+// (s_tok[r], when given, holds that token for sorted row r);
 // step 4 reads sorted row r from cache slot r - slot_base or, when vin is
 // given, straight from vin[r][K] in global memory.
 template <int MODE, int L, int RU, int GT, int NT>
@@ -107,7 +108,7 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
                                             float (&acc)[RU][DecTraits<MODE, L, RU>::nmat][kDecPass],
                                             const Cursor &c, const int *s_pairs, const uint8_t *xcb,
                                             int slot_base, const __half *vin, const TaskDims &a,
-                                            int lane) {
+                                            int lane, const int *s_tok = nullptr) {
     using Tr = DecTraits<MODE, L, RU>;
     constexpr int nmat = Tr::nmat;
     constexpr int CH = NT == 1 ? 4 : (NT == 2 ? 2 : 1);  // independent chains per product sum
@@ -119,8 +120,17 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const int r = c.r0 + c.tb + t;
-        const int p = s_pairs[r];
-        const int slot = MODE == kDecGateUp ? ((p >= 0 && p < a.P) ? p / a.k : 0) : r - slot_base;
+        int slot;
+        if (MODE == kDecGateUp) {
+            if (s_tok) {
+                slot = s_tok[r];
+            } else {
+                const int p = s_pairs[r];
+                slot = (p >= 0 && p < a.P) ? p / a.k : 0;
+            }
+        } else {
+            slot = r - slot_base;
+        }
         xb[t] = xcb + (size_t)slot * 4 * G * 16 + ks * 16;
     }
     uint32_t soff[nmat], zoff[nmat];
@@ -128,9 +138,12 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
 #pragma unroll
     for (int b = 0; b < nmat; ++b) {
         nfirst[b] = c.unit0 + b * a.rows;
-        const WarpCopy cp = warp_copy(c.e, nfirst[b], c.cnt, a.N, K);
-        soff[b] = nmat * wg.q_bytes + b * wg.s_bytes + cp.s_skip;
-        zoff[b] = nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes + cp.z_skip;
+        // the copies' 16-byte widening: only the low four bits of the byte
+        // offsets matter, so 32-bit products (wrapping) give them exactly
+        const uint32_t row = (uint32_t)c.e * (uint32_t)a.N + (uint32_t)nfirst[b];
+        const uint32_t zrow = (uint32_t)c.e * (uint32_t)(a.N / 8) + (uint32_t)(nfirst[b] / 8);
+        soff[b] = nmat * wg.q_bytes + b * wg.s_bytes + ((row * (uint32_t)G * 2u) & 15u);
+        zoff[b] = nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes + ((zrow * (uint32_t)G * 4u) & 15u);
     }
 #pragma unroll
     for (int ru = 0; ru < RU; ++ru) {

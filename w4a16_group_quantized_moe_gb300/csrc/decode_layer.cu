@@ -22,13 +22,11 @@ LayerPlan layer_plan(int T, int E, int k, int H, int I, int num_sms, size_t smem
     const int RT1 = 32 / pl.L1, RT2 = 2 * (32 / pl.L2);
     const uint32_t b1 = warp_geom(RT1, 2, H).bytes, b2 = warp_geom(RT2, 1, I).bytes;
     pl.slot_bytes = b1 > b2 ? b1 : b2;
-    // h rows one CTA's down share can read: its experts (at most the tasks
-    // over the tasks per expert, plus one) times T rows each
-    const int TPE2 = (H + RT2 - 1) / RT2;
-    const long long Amax = P < E ? P : E;
-    const long long per_cta = (Amax * TPE2 + num_sms - 1) / num_sms;
-    const long long experts = (per_cta + TPE2 - 1) / TPE2 + 1;
-    long long hr = experts * T;
+    // h rows one CTA's down share can read.  Shares are contiguous runs of
+    // tasks of equal weight, a task of expert a weighing (2 + rows of a), so
+    // the experts wholly inside a share hold at most 3P/NC + 1 rows; the two
+    // experts cut by its ends add at most T rows each.
+    const long long hr = (3LL * P + num_sms - 1) / num_sms + 1 + 2LL * T;
     pl.hrows = (int)(hr < P ? hr : P);
     for (int nw = kLayerMaxWarps; nw >= kLayerMinWarps; --nw) {
         if (nw <= T) break;  // warps beyond the T routing warps stage x

@@ -86,8 +86,8 @@ __host__ __device__ inline LayerLayout layer_layout(int T, int H, int I, int P, 
                                                     uint32_t slot_bytes) {
     LayerLayout L;
     L.meta = 0;
-    L.blk = (uint32_t)align_up((size_t)(10 * P + 8) * 4, 128);
-    L.cache = L.blk + (uint32_t)align_up((size_t)(2 * (H / 8)) * 4, 128);
+    L.blk = (uint32_t)align_up((size_t)(11 * P + 8) * 4, 128);
+    L.cache = L.blk + (uint32_t)align_up((size_t)(H / 8) * 4, 128);
     const size_t xc = (size_t)T * H * 2, hc = (size_t)hrows * I * 2;
     L.ring = L.cache + (uint32_t)align_up(xc > hc ? xc : hc, 128);
     L.bars = L.ring + (uint32_t)nw * kLayerSlots * slot_bytes;
@@ -168,6 +168,38 @@ __device__ __forceinline__ void layer_finish_down(float (&acc)[2][1][kDecPass], 
         for (int t = 0; t < kDecPass; ++t) acc[ru][0][t] = 0.f;
 }
 
+// Position of a task in one of the two flat task lists (expert-major): the
+// active slot and the task's index within that expert.
+struct TaskPos {
+    int ai, li;
+};
+
+// Advances a position by `step` tasks in a list of tpe tasks per expert.
+__device__ __forceinline__ void task_advance(TaskPos &p, int step, int tpe) {
+    p.li += step;
+    while (p.li >= tpe) {
+        p.li -= tpe;
+        ++p.ai;
+    }
+}
+
+// First task of a CTA's share: tasks are weighted by (2 + rows of their
+// expert's segment), the dequantisation being worth about two rows of
+// products, and CTA c owns the tasks whose weighted start lies in
+// [c W / NC, (c+1) W / NC).  The weighted start of expert a's first task is
+// tpe * (2 a + lo[a]) (lo: first sorted row of the segment).
+__device__ __forceinline__ void share_start(long long w, int A, int tpe, const int *s_lo, const int *s_hi,
+                                            int *s_out, int tid, int nth) {
+    for (int a = tid; a < A; a += nth) {
+        const long long pa = (long long)tpe * (2 * a + s_lo[a]);
+        const long long pn = (long long)tpe * (2 * (a + 1) + s_hi[a]);
+        if (pa <= w && w < pn) {
+            const long long cost = 2 + s_hi[a] - s_lo[a];
+            *s_out = a * tpe + (int)((w - pa + cost - 1) / cost);
+        }
+    }
+}
+
 template <int L1, int GT1, int L2, int GT2>
 __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(const LayerArgs a) {
     using T1 = DecTraits<kDecGateUp, L1, 1>;
@@ -189,20 +221,22 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     int *g_less = s_cnt1 + P;   // grouping scratch per pair
     int *g_same = g_less + P;
     int *g_first = g_same + P;
-    int *s_misc = g_first + P;  // [0] A, [1] completed blocks, [2] h not ready
-    int *s_blk = reinterpret_cast<int *>(smem + Ly.blk);  // [nblk] counts, [nblk] completed list
+    int *s_tok = g_first + P;   // token of each sorted row
+    volatile int *s_misc = s_tok + P;  // [0] A, [2] h not ready, [3] give up, [4..7] share bounds
+    int *s_blk = reinterpret_cast<int *>(smem + Ly.blk);  // [nblk] rows counted per output block
     uint8_t *cache = smem + Ly.cache;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *ring = smem + Ly.ring + (size_t)warp * kLayerSlots * a.slot_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * kLayerSlots;
     const WarpGeom wg1 = warp_geom(RT1, 2, H), wg2 = warp_geom(RT2, 1, I);
+    const int cta = blockIdx.x, NC = gridDim.x;
 
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kLayerSlots; ++s) mbar_init(bars + s, 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < 2 * nblk; i += NTH) s_blk[i] = 0;
+    for (int i = tid; i < nblk; i += NTH) s_blk[i] = 0;
     for (int i = tid; i < P; i += NTH) s_cnt1[i] = 0;
     if (tid < 8) s_misc[tid] = 0;
     pdl_wait();
@@ -210,9 +244,16 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
 
     // ---- 1. route (warps < T) while the other warps stage the x rows
     if (warp < a.T) {
-        const bool lead = blockIdx.x == 0;
-        route_token<kLayerRoutePer>(a.logits + (size_t)warp * a.E, a.E, k, warp, lead ? a.topk_ids : nullptr,
-                                    lead ? a.topk_w : nullptr, s_ids, s_w);
+        const bool lead = cta == 0;
+        const float *row = a.logits + (size_t)warp * a.E;
+        int32_t *ids = lead ? a.topk_ids : nullptr;
+        float *w = lead ? a.topk_w : nullptr;
+        if (a.E <= 128)
+            route_token<4>(row, a.E, k, warp, ids, w, s_ids, s_w);
+        else if (a.E <= 512)
+            route_token<16>(row, a.E, k, warp, ids, w, s_ids, s_w);
+        else
+            route_token<32>(row, a.E, k, warp, ids, w, s_ids, s_w);
     } else if (NTH > 32 * a.T) {  // the host keeps NW > T
         dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
     }
@@ -229,10 +270,11 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             before += (f == e) & (q < p);
         }
         s_pairs[less + before] = p;
+        s_tok[less + before] = p / k;
         g_less[p] = less;
         g_same[p] = same;
         g_first[p] = before == 0;
-        if (before == 0) atomicAdd(&s_misc[0], 1);
+        if (before == 0) atomicAdd(const_cast<int *>(&s_misc[0]), 1);
     }
     __syncthreads();
     for (int p = tid; p < P; p += NTH) {
@@ -246,75 +288,90 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     }
     __syncthreads();
 
-    // ---- 2. this CTA's tasks: contiguous shares of both task lists
+    // ---- 2. this CTA's shares of both task lists (weighted, contiguous)
     const int A = s_misc[0];
     const int TPE1 = (I + RT1 - 1) / RT1, TPE2 = (H + RT2 - 1) / RT2;
-    const int U1 = A * TPE1, U2 = A * TPE2;
-    const int cta = blockIdx.x, NC = gridDim.x;
-    const int b1 = (int)((long long)U1 * cta / NC), e1 = (int)((long long)U1 * (cta + 1) / NC);
-    const int b2 = (int)((long long)U2 * cta / NC), e2 = (int)((long long)U2 * (cta + 1) / NC);
+    {
+        const long long W1 = (long long)TPE1 * (2 * A + P), W2 = (long long)TPE2 * (2 * A + P);
+        if (tid == 0) {
+            s_misc[4] = 0; s_misc[5] = A * TPE1; s_misc[6] = 0; s_misc[7] = A * TPE2;
+        }
+        __syncthreads();
+        int *sm = const_cast<int *>(s_misc);
+        share_start(W1 * cta / NC, A, TPE1, s_lo, s_hi, sm + 4, tid, NTH);
+        if (cta + 1 < NC) share_start(W1 * (cta + 1) / NC, A, TPE1, s_lo, s_hi, sm + 5, tid, NTH);
+        share_start(W2 * cta / NC, A, TPE2, s_lo, s_hi, sm + 6, tid, NTH);
+        if (cta + 1 < NC) share_start(W2 * (cta + 1) / NC, A, TPE2, s_lo, s_hi, sm + 7, tid, NTH);
+        __syncthreads();
+    }
+    const int b1 = s_misc[4], e1 = s_misc[5], b2 = s_misc[6], e2 = s_misc[7];
+    // this warp's tasks: b1 + warp + i*NW (i < n1), then b2 + warp + j*NW
     const int n1 = e1 - b1 > warp ? (e1 - b1 - warp + NW - 1) / NW : 0;
     const int n2 = e2 - b2 > warp ? (e2 - b2 - warp + NW - 1) / NW : 0;
     const int ntask = n1 + n2;
 
-    auto cursor = [&](int i, Cursor &cu) -> int {  // returns the active slot
-        int ai;
-        if (i < n1) {
-            const int uu = b1 + warp + i * NW;
-            ai = uu / TPE1;
-            cu.unit0 = (uu - ai * TPE1) * RT1;
-            cu.cnt = min(RT1, I - cu.unit0);
-        } else {
-            const int uu = b2 + warp + (i - n1) * NW;
-            ai = uu / TPE2;
-            cu.unit0 = (uu - ai * TPE2) * RT2;
-            cu.cnt = min(RT2, H - cu.unit0);
-        }
-        cu.e = s_act[ai];
-        cu.r0 = s_lo[ai];
-        cu.ne = s_hi[ai] - cu.r0;
+    // positions of the next task to issue and of the two tasks in the slots
+    int iss = 0;
+    TaskPos ip{(b1 + warp) / TPE1, (b1 + warp) % TPE1};
+    if (n1 == 0) ip = TaskPos{(b2 + warp) / TPE2, (b2 + warp) % TPE2};
+    TaskPos q0{0, 0}, q1{0, 0};  // tasks in flight, oldest first
+
+    auto make_cursor = [&](const TaskPos &tp, bool gate, Cursor &cu) {
+        const int rt = gate ? RT1 : RT2, rows = gate ? I : H;
+        cu.unit0 = tp.li * rt;
+        cu.cnt = min(rt, rows - cu.unit0);
+        cu.e = s_act[tp.ai];
+        cu.r0 = s_lo[tp.ai];
+        cu.ne = s_hi[tp.ai] - cu.r0;
         cu.tb = 0;
-        return ai;
     };
-    // lane 0 fetches task i into slot i % kLayerSlots
-    auto issue = [&](int i) {
-        if (lane != 0) return;
+    // fetch task `iss` (position ip) into slot iss % 2, then advance ip.
+    // Lane 0 posts the expected bytes; lanes 0-5 (gate/up: codes, scales,
+    // zeros of gate and up) or 0-2 (down) then issue one bulk copy each.
+    auto issue = [&]() {
+        const bool gate = iss < n1;
         Cursor cu;
-        cursor(i, cu);
-        uint8_t *wb = ring + (size_t)(i % kLayerSlots) * a.slot_bytes;
-        uint64_t *bar = bars + i % kLayerSlots;
-        fence_proxy_async();  // this warp's earlier reads of the slot come first
-        if (i < n1) {
-            WarpCopy cp[2];
-            uint32_t tx = 0;
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                cp[b] = warp_copy(cu.e, cu.unit0 + b * I, cu.cnt, 2 * I, H);
-                tx += cp[b].q_len + cp[b].s_len + cp[b].z_len;
+        make_cursor(ip, gate, cu);
+        uint8_t *wb = ring + (size_t)(iss % kLayerSlots) * a.slot_bytes;
+        uint64_t *bar = bars + iss % kLayerSlots;
+        const int nmat = gate ? 2 : 1;
+        const int N = gate ? 2 * I : H, K = gate ? H : I;
+        const WarpGeom &wg = gate ? wg1 : wg2;
+        const int b = lane % nmat, kind = lane / nmat;  // kind 0 codes, 1 scales, 2 zeros
+        const WarpCopy cp = warp_copy(cu.e, cu.unit0 + b * I, cu.cnt, N, K);
+        uint32_t tx = cp.q_len + cp.s_len + cp.z_len;
+        if (gate) tx += __shfl_xor_sync(0xffffffffu, tx, 1);
+        if (lane == 0) mbar_arrive_expect_tx(bar, tx);
+        __syncwarp();
+        if (kind < 3) {
+            fence_proxy_async();  // this warp's earlier reads of the slot come first
+            const uint8_t *src;
+            uint32_t dst, len;
+            if (kind == 0) {
+                src = reinterpret_cast<const uint8_t *>(gate ? (const void *)a.q13 : (const void *)a.q2) + cp.q_off;
+                dst = b * wg.q_bytes;
+                len = cp.q_len;
+            } else if (kind == 1) {
+                src = reinterpret_cast<const uint8_t *>(gate ? (const void *)a.s13 : (const void *)a.s2) + cp.s_a;
+                dst = nmat * wg.q_bytes + b * wg.s_bytes;
+                len = cp.s_len;
+            } else {
+                src = reinterpret_cast<const uint8_t *>(gate ? (const void *)a.z13 : (const void *)a.z2) + cp.z_a;
+                dst = nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes;
+                len = cp.z_len;
             }
-            mbar_arrive_expect_tx(bar, tx);
-#pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                bulk_g2s(wb + b * wg1.q_bytes, reinterpret_cast<const uint8_t *>(a.q13) + cp[b].q_off,
-                         cp[b].q_len, bar);
-                bulk_g2s(wb + 2 * wg1.q_bytes + b * wg1.s_bytes,
-                         reinterpret_cast<const uint8_t *>(a.s13) + cp[b].s_a, cp[b].s_len, bar);
-                bulk_g2s(wb + 2 * (wg1.q_bytes + wg1.s_bytes) + b * wg1.z_bytes,
-                         reinterpret_cast<const uint8_t *>(a.z13) + cp[b].z_a, cp[b].z_len, bar);
-            }
-        } else {
-            const WarpCopy cp = warp_copy(cu.e, cu.unit0, cu.cnt, H, I);
-            mbar_arrive_expect_tx(bar, cp.q_len + cp.s_len + cp.z_len);
-            bulk_g2s(wb, reinterpret_cast<const uint8_t *>(a.q2) + cp.q_off, cp.q_len, bar);
-            bulk_g2s(wb + wg2.q_bytes, reinterpret_cast<const uint8_t *>(a.s2) + cp.s_a, cp.s_len, bar);
-            bulk_g2s(wb + wg2.q_bytes + wg2.s_bytes, reinterpret_cast<const uint8_t *>(a.z2) + cp.z_a,
-                     cp.z_len, bar);
+            bulk_g2s(wb + dst, src, len, bar);
         }
+        // record and advance (every lane keeps the same positions)
+        if (iss == 0) q0 = ip; else q1 = ip;
+        ++iss;
+        if (iss == n1) ip = TaskPos{(b2 + warp) / TPE2, (b2 + warp) % TPE2};
+        else task_advance(ip, NW, iss < n1 ? TPE1 : TPE2);
     };
 
     const int nfirst = ntask < kLayerSlots ? ntask : kLayerSlots;
-    for (int i = 0; i < nfirst; ++i) issue(i);
-    int issued = nfirst, consumed = 0;
+    for (int i = 0; i < nfirst; ++i) issue();
+    int consumed = 0;
 
     const TaskDims td1{2 * I, H, I, P, k}, td2{H, I, H, P, k};
     float acc1[1][2][kDecPass], acc2[2][1][kDecPass];
@@ -384,51 +441,43 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         }
         consumed = i + 1;
         const uint8_t *wb = ring + (size_t)s * a.slot_bytes;
+        const TaskPos tp = q0;
+        q0 = q1;
         Cursor cu;
-        const int ai = cursor(i, cu);
+        make_cursor(tp, i < n1, cu);
         if (i < n1) {
-            for (cu.tb = 0; cu.tb < cu.ne; cu.tb += kDecPass) {
-                const int nt = min(kDecPass, cu.ne - cu.tb);
-                switch (nt) {
-                    case 1:
-                        dec_compute<kDecGateUp, L1, 1, GT1, 1>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane);
-                        layer_finish_gate_up<L1, 1>(acc1, cu, a, G2, lane);
-                        break;
-                    case 2:
-                        dec_compute<kDecGateUp, L1, 1, GT1, 2>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane);
-                        layer_finish_gate_up<L1, 2>(acc1, cu, a, G2, lane);
-                        break;
-                    case 3:
-                        dec_compute<kDecGateUp, L1, 1, GT1, 3>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane);
-                        layer_finish_gate_up<L1, 3>(acc1, cu, a, G2, lane);
-                        break;
-                    default:
-                        dec_compute<kDecGateUp, L1, 1, GT1, 4>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane);
-                        layer_finish_gate_up<L1, 4>(acc1, cu, a, G2, lane);
-                        break;
+            for (cu.tb = 0; cu.tb < cu.ne;) {
+                const int nt = cu.ne - cu.tb;
+                if (nt >= 4) {
+                    dec_compute<kDecGateUp, L1, 1, GT1, 4>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok);
+                    layer_finish_gate_up<L1, 4>(acc1, cu, a, G2, lane);
+                    cu.tb += 4;
+                } else if (nt >= 2) {
+                    dec_compute<kDecGateUp, L1, 1, GT1, 2>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok);
+                    layer_finish_gate_up<L1, 2>(acc1, cu, a, G2, lane);
+                    cu.tb += 2;
+                } else {
+                    dec_compute<kDecGateUp, L1, 1, GT1, 1>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok);
+                    layer_finish_gate_up<L1, 1>(acc1, cu, a, G2, lane);
+                    cu.tb += 1;
                 }
             }
-            if (lane == 0) atomicAdd(&s_cnt1[ai], cu.cnt);
+            if (lane == 0) atomicAdd(&s_cnt1[tp.ai], cu.cnt);
         } else {
-            for (cu.tb = 0; cu.tb < cu.ne; cu.tb += kDecPass) {
-                const int nt = min(kDecPass, cu.ne - cu.tb);
-                switch (nt) {
-                    case 1:
-                        dec_compute<kDecDown, L2, 2, GT2, 1>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
-                        layer_finish_down<L2, 1>(acc2, cu, s_pairs, a, lane);
-                        break;
-                    case 2:
-                        dec_compute<kDecDown, L2, 2, GT2, 2>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
-                        layer_finish_down<L2, 2>(acc2, cu, s_pairs, a, lane);
-                        break;
-                    case 3:
-                        dec_compute<kDecDown, L2, 2, GT2, 3>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
-                        layer_finish_down<L2, 3>(acc2, cu, s_pairs, a, lane);
-                        break;
-                    default:
-                        dec_compute<kDecDown, L2, 2, GT2, 4>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
-                        layer_finish_down<L2, 4>(acc2, cu, s_pairs, a, lane);
-                        break;
+            for (cu.tb = 0; cu.tb < cu.ne;) {
+                const int nt = cu.ne - cu.tb;
+                if (nt >= 4) {
+                    dec_compute<kDecDown, L2, 2, GT2, 4>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
+                    layer_finish_down<L2, 4>(acc2, cu, s_pairs, a, lane);
+                    cu.tb += 4;
+                } else if (nt >= 2) {
+                    dec_compute<kDecDown, L2, 2, GT2, 2>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
+                    layer_finish_down<L2, 2>(acc2, cu, s_pairs, a, lane);
+                    cu.tb += 2;
+                } else {
+                    dec_compute<kDecDown, L2, 2, GT2, 1>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
+                    layer_finish_down<L2, 1>(acc2, cu, s_pairs, a, lane);
+                    cu.tb += 1;
                 }
             }
             if (lane == 0) {
@@ -438,45 +487,53 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             }
         }
         __syncwarp();
-        if (issued < ntask) issue(issued++);
+        if (iss < ntask) issue();
     }
     // never leave with a copy in flight into this CTA's shared memory
-    for (int j = consumed; j < issued; ++j)
+    for (int j = consumed; j < iss; ++j)
         mbar_wait_bounded(bars + j % kLayerSlots, (uint32_t)((j / kLayerSlots) & 1), nullptr);
 
-    // ---- 4. publish row counts; combine the blocks this CTA completes
+    // ---- 4. publish this CTA's row counts per output block, then combine
+    // this CTA's slice of blocks once every active expert's rows are in
     __syncthreads();
-    int *s_done = s_blk + nblk;
     if (!dead) {
         for (int nb = tid; nb < nblk; nb += NTH) {
             const int c = s_blk[nb];
             if (c == 0) continue;
             __threadfence();
-            const unsigned old = atomicAdd(a.blkctr + nb, (unsigned)c);
-            if (old + c == (unsigned)A * 8u) {
-                __threadfence();
-                s_done[atomicAdd(&s_misc[1], 1)] = nb;
-            }
+            atomicAdd(a.blkctr + nb, (unsigned)c);
         }
     }
-    __syncthreads();
-    const int ndone = s_misc[1];
-    if (ndone > 0) __threadfence();
-    for (int d = warp; d < ndone; d += NW) {
-        const int nb = s_done[d];
-        for (int idx = lane; idx < a.T * 8; idx += 32) {
-            const int t = idx >> 3, n = nb * 8 + (idx & 7);
-            float accv = 0.f;
-#pragma unroll 8
-            for (int j = 0; j < k; ++j) {  // unrolled: the loads go out together
-                const int p = t * k + j;
-                accv = fmaf(s_w[p], __ldcg(a.y + (size_t)p * H + n), accv);
+    const int q_lo = (int)((long long)nblk * cta / NC), q_hi = (int)((long long)nblk * (cta + 1) / NC);
+    const int units = (q_hi - q_lo) * a.T;  // (block, token) pairs
+    const int o = lane & 7, js = lane >> 3;
+    for (int u = warp; u < units; u += NW) {
+        const int nb = q_lo + u / a.T, t = u - (u / a.T) * a.T;
+        if (s_misc[3]) break;  // an earlier wait of this CTA expired
+        // every lane waits (acquire) for all rows of the block
+        uint32_t it = 0;
+        while (ld_acquire_u32(a.blkctr + nb) < (uint32_t)A * 8u && ++it < kPollTries) __nanosleep(64);
+        if (__any_sync(0xffffffffu, it >= kPollTries)) {
+            if (lane == 0) {
+                set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
+                s_misc[3] = 1;
             }
-            a.out[(size_t)t * H + n] = __float2half_rn(accv);
+            break;
         }
-        __syncwarp();
-        if (lane == 0) atomicExch(a.blkctr + nb, 0u);
+        // out[t][n] = sum_j w[t][j] y[t*k+j][n]: lanes (o, js) sum j = js, js+4, ...,
+        // then a fixed shuffle tree over js (deterministic order)
+        const int n = nb * 8 + o;
+        float accv = 0.f;
+        for (int j = js; j < k; j += 4) {
+            const int p = t * k + j;
+            accv = fmaf(s_w[p], __ldcg(a.y + (size_t)p * H + n), accv);
+        }
+        accv += __shfl_xor_sync(0xffffffffu, accv, 8);
+        accv += __shfl_xor_sync(0xffffffffu, accv, 16);
+        if (js == 0) a.out[(size_t)t * H + n] = __float2half_rn(accv);
     }
+    __syncthreads();  // every poll of this CTA's blocks is done
+    for (int nb = q_lo + tid; nb < q_hi; nb += NTH) a.blkctr[nb] = 0u;
 
     // ---- the last CTA to leave resets the per-expert counters
     __syncthreads();

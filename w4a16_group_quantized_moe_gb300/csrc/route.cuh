@@ -17,6 +17,31 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) + 1u;
 }
 
+// The largest untaken key of a lane and its slot (the lowest slot among
+// equal keys), by a pairwise tree: blocks of 2, 4, ... slots, the right block
+// winning only when strictly larger, so the depth is log2(PER), not PER.
+template <int PER>
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[PER], uint32_t taken, uint32_t &bk,
+                                          int &bj) {
+    uint32_t kk[PER];
+    int jj[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        kk[j] = ((taken >> j) & 1u) ? 0u : key[j];
+        jj[j] = j;
+    }
+#pragma unroll
+    for (int st = 1; st < PER; st *= 2)
+#pragma unroll
+        for (int j = 0; j + st < PER; j += 2 * st) {
+            const bool r = kk[j + st] > kk[j];
+            kk[j] = r ? kk[j + st] : kk[j];
+            jj[j] = r ? jj[j + st] : jj[j];
+        }
+    bk = kk[0];
+    bj = jj[0];
+}
+
 // Routes one token with one warp.  PER = logits held per lane (E <= 32*PER).
 // Writes ids and weights of token t to every destination given (non-null):
 // topk_ids / topk_w at [t*k + j], and s_ids / s_w at [t*k + j].
@@ -32,14 +57,9 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
         key[j] = e < E ? order_key(__ldg(row + e)) : 0u;
     }
     // this lane's best untaken candidate (first maximum in index order)
-    uint32_t bk = 0, taken = 0;
-    int bj = 0;
-#pragma unroll
-    for (int j = 0; j < PER; ++j)
-        if (key[j] > bk) {
-            bk = key[j];
-            bj = j;
-        }
+    uint32_t bk, taken = 0;
+    int bj;
+    lane_best<PER>(key, taken, bk, bj);
 
     int my_id = 0;  // lane s keeps the s-th selection
     for (int s = 0; s < k; ++s) {
@@ -49,16 +69,7 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
         if (lane == s) my_id = win;
         if ((win & 31) == lane) {
             taken |= 1u << (win >> 5);
-            bk = 0;
-            bj = 0;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const uint32_t c = ((taken >> j) & 1u) ? 0u : key[j];
-                if (c > bk) {
-                    bk = c;
-                    bj = j;
-                }
-            }
+            lane_best<PER>(key, taken, bk, bj);
         }
     }
 
