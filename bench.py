@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--flush-mb", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="weight copies used in turn (0: enough to exceed L2 twice; 1 for profiling)")
     return ap.parse_args()
 
 
@@ -260,7 +262,7 @@ def main():
     # workload here -- and each step reads its weights from HBM.
     b = inputs.bytes_per_expert(H, I)
     per_step = min(E, T * k) * (b["w13"] + b["w2"])
-    NL = max(4, min(16, int(np.ceil(2 * 126e6 / max(per_step, 1))) + 1))
+    NL = args.layers if args.layers > 0 else max(4, min(16, int(np.ceil(2 * 126e6 / max(per_step, 1))) + 1))
     layers = [moe.MoELayer(dw13, dw2, T, k, device=dev)]
     for _ in range(NL - 1):
         c13 = tuple(t.clone() for t in dw13)

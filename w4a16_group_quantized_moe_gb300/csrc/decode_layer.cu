@@ -22,6 +22,8 @@ LayerPlan layer_plan(int T, int E, int k, int H, int I, int num_sms, size_t smem
     const int RT1 = 32 / pl.L1, RT2 = 2 * (32 / pl.L2);
     const uint32_t b1 = warp_geom(RT1, 2, H).bytes, b2 = warp_geom(RT2, 1, I).bytes;
     pl.slot_bytes = b1 > b2 ? b1 : b2;
+    // the router keeps E keys in a routing warp's ring before any copy
+    if ((size_t)kLayerSlots * pl.slot_bytes < (size_t)E * 4) pl.slot_bytes = (uint32_t)align_up((size_t)E * 4 / kLayerSlots, 128);
     // h rows one CTA's down share can read.  Shares are contiguous runs of
     // tasks of equal weight, a task of expert a weighing (2 + rows of a), so
     // the experts wholly inside a share hold at most 3P/NC + 1 rows; the two

@@ -248,12 +248,8 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         const float *row = a.logits + (size_t)warp * a.E;
         int32_t *ids = lead ? a.topk_ids : nullptr;
         float *w = lead ? a.topk_w : nullptr;
-        if (a.E <= 128)
-            route_token<4>(row, a.E, k, warp, ids, w, s_ids, s_w);
-        else if (a.E <= 512)
-            route_token<16>(row, a.E, k, warp, ids, w, s_ids, s_w);
-        else
-            route_token<32>(row, a.E, k, warp, ids, w, s_ids, s_w);
+        // keys in this warp's task ring, which no copy has touched yet
+        route_token_compact(row, a.E, k, warp, ids, w, s_ids, s_w, reinterpret_cast<uint32_t *>(ring));
     } else if (NTH > 32 * a.T) {  // the host keeps NW > T
         dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
     }

@@ -89,4 +89,56 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
     }
 }
 
+// The same routing as route_token, written for a cold instruction cache: a
+// kernel that routes once per launch runs this code once, and each 128-byte
+// line of straight-line code costs an L2 round trip on first use, so the
+// selection is a short loop over keys kept in shared memory (s_key: E
+// words of this warp) instead of unrolled register code.  Each of the k
+// rounds scans the lane's keys in ascending expert order (first maximum =
+// lowest index), takes the warp maximum and, among lanes holding it, the
+// lowest expert index; the winner's key is cleared.  Results are identical
+// to route_token's.
+__device__ __forceinline__ void route_token_compact(const float *__restrict__ row, int E, int k, int t,
+                                                    int32_t *__restrict__ topk_ids,
+                                                    float *__restrict__ topk_w, int *s_ids, float *s_w,
+                                                    uint32_t *s_key) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 4
+    for (int e = lane; e < E; e += 32) s_key[e] = order_key(__ldg(row + e));
+    __syncwarp();
+    int my_id = 0;
+    for (int s = 0; s < k; ++s) {
+        // two interleaved scans (even and odd strides), merged keeping the lower index on ties
+        uint32_t b0 = 0, b1 = 0;
+        int e0 = 0x7fffffff, e1 = 0x7fffffff;
+        for (int e = lane; e < E; e += 64) {
+            const uint32_t v0 = s_key[e];
+            if (v0 > b0) { b0 = v0; e0 = e; }
+            if (e + 32 < E) {
+                const uint32_t v1 = s_key[e + 32];
+                if (v1 > b1) { b1 = v1; e1 = e + 32; }
+            }
+        }
+        if (b1 > b0 || (b1 == b0 && e1 < e0)) { b0 = b1; e0 = e1; }
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, b0);
+        const int win = (int)__reduce_min_sync(0xffffffffu, b0 == kmax ? (uint32_t)e0 : 0xffffffffu);
+        if (lane == s) my_id = win;
+        if (lane == (win & 31)) s_key[win] = 0u;
+        __syncwarp();
+    }
+    const float my_logit = lane < k ? __ldg(row + my_id) : 0.f;
+    const float m = __shfl_sync(0xffffffffu, my_logit, 0);
+    const float ex = (lane < k) ? expf(my_logit - m) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < k) {
+        const float w = ex / sum;
+        if (topk_ids) topk_ids[(size_t)t * k + lane] = my_id;
+        if (topk_w) topk_w[(size_t)t * k + lane] = w;
+        if (s_ids) s_ids[t * k + lane] = my_id;
+        if (s_w) s_w[t * k + lane] = w;
+    }
+}
+
 }  // namespace moe
