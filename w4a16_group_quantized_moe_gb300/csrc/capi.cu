@@ -34,6 +34,13 @@ cudaError_t launch_down_decode(const __half *, const uint32_t *, const __half *,
                                const float *, int, int, int, int, int, __half *, float *, uint32_t *,
                                uint32_t *, int, size_t, cudaStream_t);
 
+bool tc_supported(int, int, int, int, int, size_t);
+cudaError_t launch_gate_up_tc(const __half *, const uint32_t *, const __half *, const uint32_t *,
+                              const int32_t *, const int32_t *, const int32_t *, const int32_t *, int, int,
+                              int, int, int, __half *, uint32_t *, int, size_t, cudaStream_t);
+cudaError_t launch_down_tc(const __half *, const uint32_t *, const __half *, const uint32_t *,
+                           const int32_t *, const int32_t *, const int32_t *, const int32_t *, const float *,
+                           int, int, int, int, int, __half *, float *, uint32_t *, int, size_t, cudaStream_t);
 bool layer_fusable(int, int, int, int, int, int, size_t);
 cudaError_t launch_decode_layer(const float *, const __half *, const uint32_t *, const __half *,
                                 const uint32_t *, const uint32_t *, const __half *, const uint32_t *,
@@ -221,6 +228,11 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
             reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,
             expert_offsets, sorted_pair, active_experts, num_active, T, E, k, H, I,
             reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
+    if (tc_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_gate_up_tc(
+            reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,
+            expert_offsets, sorted_pair, active_experts, num_active, T, E, k, H, I,
+            reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
     e = launch_gate_up_stream(reinterpret_cast<const __half *>(x), w13_q,
                               reinterpret_cast<const __half *>(w13_s), w13_z, expert_offsets,
                               sorted_pair, active_experts, num_active, T, E, k, H, I,
@@ -257,6 +269,12 @@ MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, c
             expert_offsets, sorted_pair, active_experts, num_active, topk_w, T, E, k, H, I,
             reinterpret_cast<__half *>(out), reinterpret_cast<float *>(ws + L.y),
             reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms, di.smem_optin,
+            static_cast<cudaStream_t>(stream)));
+    if (tc_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_down_tc(
+            reinterpret_cast<const __half *>(h), w2_q, reinterpret_cast<const __half *>(w2_s), w2_z,
+            expert_offsets, sorted_pair, active_experts, num_active, topk_w, T, E, k, H, I,
+            reinterpret_cast<__half *>(out), reinterpret_cast<float *>(ws + L.y), err, di.sms, di.smem_optin,
             static_cast<cudaStream_t>(stream)));
     e = launch_down_stream(reinterpret_cast<const __half *>(h), w2_q,
                            reinterpret_cast<const __half *>(w2_s), w2_z, expert_offsets, sorted_pair,

@@ -1,0 +1,592 @@
+// prefill_tc.cu -- steps 3 and 4 for large batches on the 5th-generation
+// tensor cores (tcgen05 MMA, accumulators in tensor memory).
+//
+// With thousands of tokens every expert sees tens to hundreds of rows, so
+// the per-expert products of "Sparse MoE layer" (gate/up + SiLU, down) are
+// dense contractions: for expert e, D[n][r] = sum_K W_e[n][K] * act[r][K]
+// over the weight rows n of a 128-row tile and the (up to 128) activation
+// rows r of a chunk of e's segment.  The weight is the MMA's A operand
+// (M = 128 rows), the gathered activation rows its B operand (N = the chunk,
+// padded to 16): the grouping of "Active grouped decode" (active-expert
+// segments with offsets) decides the work list, and no expert is padded
+// beyond one 16-row MMA granule.
+//
+// One persistent CTA per SM, warp-specialised, all stages in shared memory:
+//   warp 0      bulk tensor copies (TMA) of the packed codes of each 64-wide
+//               K block (gate and up tiles, or the down tile)
+//   warps 2-9   dequantise the codes to fp16 ((q - z) * s, per 32-wide
+//               group, exact q - z from the binary16 exponent trick) into
+//               the 128-byte-swizzled K-major operand layout, and gather the
+//               activation rows of the chunk into the same layout (both in
+//               the pair order [k0 k4 k1 k5 k2 k6 k3 k7] of the dequantiser:
+//               the contraction over K does not depend on the order)
+//   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate in
+//               tensor memory) for each K block and commits to mbarriers
+//   warps 10-13 read the accumulators (tcgen05.ld) and finish: h =
+//               silu(gate) * up in fp16 (step 3), or the fp32 per-pair
+//               projection y (step 4, summed per token by combine_kernel)
+// Stages rotate through a ring (codes -> dequantised operands -> MMA) and
+// the accumulators are double-buffered, so dequantisation, MMA and the
+// epilogue of consecutive tiles overlap.  Every wait is bounded.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kTcThreads = 448;
+constexpr int kTcProducerWarp = 0, kTcMmaWarp = 1, kTcDqWarp0 = 2, kTcDqWarps = 8;
+constexpr int kTcEpiWarp0 = 10, kTcEpiWarps = 4;
+constexpr int kTcM = 128;     // weight rows per tile
+constexpr int kTcKB = 64;     // K per stage: one 128-byte row of fp16
+constexpr int kTcMaxN = 128;  // activation rows per chunk
+constexpr int kTcMaxStages = 6;
+constexpr int kTcMinT = 64;   // smaller batches stay on the CUDA-core stream kernels
+constexpr uint32_t kTcTmemCols = 512;
+
+static_assert(kTcEpiWarp0 == kTcDqWarp0 + kTcDqWarps && (kTcEpiWarp0 + kTcEpiWarps) * 32 == kTcThreads,
+              "warp roles cover the CTA");
+
+enum { kTcGateUp = 0, kTcDown = 1 };
+
+struct TcArgs {
+    const __half *s;    // scales [E][N][G]
+    const uint32_t *z;  // zeros  [E][N/8][G]
+    const __half *vin;  // step 3: x [T][H]; step 4: h [P][I] (sorted rows)
+    int E, N, K, rows;  // N: matrix rows per expert (2I or H); rows: output rows (I or H)
+    int T, k, P;
+    const int32_t *offsets, *sorted_pair, *active, *num_active;
+    __half *h_out;      // step 3: [P][I]
+    float *y_out;       // step 4: [P][H]
+    uint32_t *err;
+    int nstages;
+};
+
+template <int MODE>
+struct TcGeom {
+    static constexpr int nmat = MODE == kTcGateUp ? 2 : 1;
+    static constexpr uint32_t a_bytes = nmat * kTcM * kTcKB * 2;  // dequantised tiles
+    static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows
+    static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes
+    static constexpr uint32_t stage = a_bytes + b_bytes + c_bytes;  // multiple of 1024
+};
+
+// Control block after the stages: mbarriers and the tensor-memory address.
+struct TcCtrl {
+    uint64_t codes_full[kTcMaxStages];
+    uint64_t dq_done[kTcMaxStages];
+    uint64_t mma_done[kTcMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem;
+    int abort;
+};
+
+__host__ __device__ inline size_t tc_smem_bytes(uint32_t stage, int nstages) {
+    return 1024 + (size_t)stage * nstages + sizeof(TcCtrl);
+}
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
+    // shared-memory matrix descriptor: K-major, 128-byte swizzle; start
+    // address >> 4, leading offset unused (1), stride offset 1024 B between
+    // 8-row groups, descriptor version 1, layout type 2 (128-byte swizzle)
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24
+__device__ __forceinline__ uint32_t tc_idesc(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// byte offset of 16-byte chunk c (K elements 8c..8c+7) of row r in a
+// 128-byte-swizzled K-major tile
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+// ---------------------------------------------------------------- work list
+// Work items, in order: for each active slot a, for each chunk of up to
+// kTcMaxN segment rows, for each 128-row weight tile.  A cursor walks them
+// with a stride (the grid), reading the routing metadata from global memory.
+struct TcItem {
+    int a, e, lo, ne, tile, chunk;  // slot, expert, first sorted row, segment rows, tile, chunk
+    bool valid;
+};
+
+struct TcWalk {
+    int a, j;        // slot and item index within the slot
+    int nitems;      // items of slot a
+    int e, lo, ne;
+};
+
+__device__ __forceinline__ bool tc_load_slot(const TcArgs &p, int A, int tiles, TcWalk &w) {
+    while (w.a < A) {
+        w.e = p.active[w.a];
+        if (w.e < 0 || w.e >= p.E) return false;
+        w.lo = p.offsets[w.e];
+        w.ne = p.offsets[w.e + 1] - w.lo;
+        w.nitems = tiles * ((w.ne + kTcMaxN - 1) / kTcMaxN);
+        if (w.j < w.nitems) return true;
+        w.j -= w.nitems;
+        ++w.a;
+    }
+    return false;
+}
+
+__device__ __forceinline__ TcItem tc_item(const TcWalk &w, int tiles, bool ok) {
+    TcItem it;
+    it.valid = ok;
+    it.a = w.a;
+    it.e = w.e;
+    it.lo = w.lo;
+    it.ne = w.ne;
+    it.chunk = w.j / tiles;
+    it.tile = w.j - it.chunk * tiles;
+    return it;
+}
+
+// ---------------------------------------------------------------- kernel
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap qmap) {
+    using Gm = TcGeom<MODE>;
+    constexpr int nmat = Gm::nmat;
+    extern __shared__ uint8_t tc_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int S = p.nstages;
+    TcCtrl *ctl = reinterpret_cast<TcCtrl *>(smem + (size_t)Gm::stage * S);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.K / 32;
+    const int nkb = (p.K + kTcKB - 1) / kTcKB;
+    const int tiles = (p.rows + kTcM - 1) / kTcM;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&ctl->codes_full[s], 1);
+            mbar_init(&ctl->dq_done[s], kTcDqWarps);
+            mbar_init(&ctl->mma_done[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&ctl->acc_full[s], 1);
+            mbar_init(&ctl->acc_empty[s], kTcEpiWarps);
+        }
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&ctl->tmem)),
+                     "r"(kTcTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem;
+    volatile int *abort_flag = &ctl->abort;
+    pdl_wait();
+    pdl_trigger();
+
+    int A = *p.num_active;
+    A = A < 0 ? 0 : (A > p.E ? p.E : A);
+    auto fail = [&](uint32_t bits) {
+        set_error(p.err, bits);
+        *abort_flag = 1;
+    };
+
+    if (warp == kTcProducerWarp) {
+        // ---- codes of every K block of every item, through the ring
+        if (lane == 0) {
+            TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
+            int j = 0;  // stage counter
+            for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag;) {
+                const TcItem it = tc_item(w, tiles, true);
+                for (int kb = 0; kb < nkb; ++kb, ++j) {
+                    const int s = j % S;
+                    if (!mbar_wait_bounded(&ctl->dq_done[s], ((j / S) & 1) ^ 1, abort_flag)) {
+                        if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                        break;
+                    }
+                    uint8_t *codes = smem + (size_t)Gm::stage * s + Gm::a_bytes + Gm::b_bytes;
+                    mbar_arrive_expect_tx(&ctl->codes_full[s], Gm::c_bytes);
+#pragma unroll
+                    for (int b = 0; b < nmat; ++b) {
+                        const int row = it.e * p.N + b * p.rows + it.tile * kTcM;
+                        tma_load_2d(codes + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row, &ctl->codes_full[s]);
+                    }
+                }
+                w.j += gridDim.x;
+                ok = tc_load_slot(p, A, tiles, w);
+            }
+            if (*abort_flag) {
+                // never leave with a copy in flight: wait for the last issue of each stage
+                for (int jj = j > S ? j - S : 0; jj < j; ++jj)
+                    mbar_wait_bounded(&ctl->codes_full[jj % S], (jj / S) & 1, nullptr);
+            }
+        }
+    } else if (warp == kTcMmaWarp) {
+        // ---- one thread issues the MMAs
+        if (lane == 0) {
+            TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
+            int j = 0, n_items = 0;
+            for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag; ++n_items) {
+                const TcItem it = tc_item(w, tiles, true);
+                const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
+                const int nmma = (nrows + 15) & ~15;
+                const uint32_t idesc = tc_idesc(nmma);
+                const int as = n_items & 1;
+                if (!mbar_wait_bounded(&ctl->acc_empty[as], ((n_items >> 1) & 1) ^ 1, abort_flag)) {
+                    if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dacc = tmem + (uint32_t)as * (nmat * kTcMaxN);
+                bool broke = false;
+                for (int kb = 0; kb < nkb; ++kb, ++j) {
+                    const int s = j % S;
+                    if (!mbar_wait_bounded(&ctl->dq_done[s], (j / S) & 1, abort_flag)) {
+                        if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                        broke = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sbase = smem_addr(smem + (size_t)Gm::stage * s);
+#pragma unroll
+                    for (int ks = 0; ks < kTcKB / 16; ++ks) {
+                        const uint64_t bd = tc_desc_sw128(sbase + Gm::a_bytes + ks * 32);
+#pragma unroll
+                        for (int b = 0; b < nmat; ++b) {
+                            const uint64_t ad = tc_desc_sw128(sbase + b * (kTcM * kTcKB * 2) + ks * 32);
+                            tc_mma(dacc + b * kTcMaxN, ad, bd, idesc, (kb | ks) != 0);
+                        }
+                    }
+                    tc_commit(&ctl->mma_done[s]);
+                }
+                if (broke) break;
+                tc_commit(&ctl->acc_full[as]);
+                w.j += gridDim.x;
+                ok = tc_load_slot(p, A, tiles, w);
+            }
+            // every MMA this thread issued has completed before tensor memory is released
+            tc_commit(&ctl->drain);
+            mbar_wait_bounded(&ctl->drain, 0, nullptr);
+        }
+    } else if (warp >= kTcDqWarp0 && warp < kTcDqWarp0 + kTcDqWarps) {
+        // ---- dequantise the codes and gather the activation rows
+        const int t = tid - kTcDqWarp0 * 32;  // 0..255
+        // A rows: step 3: matrix b = t / 128, row m = t % 128, all 8 words;
+        // step 4: row m = t % 128, words [4h, 4h+4) with h = t / 128
+        const int m = t & 127, half = t >> 7;
+        const int b = nmat == 2 ? half : 0;
+        const int w0 = nmat == 2 ? 0 : 4 * half, nw = nmat == 2 ? 8 : 4;
+        TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
+        int j = 0;
+        for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag;) {
+            const TcItem it = tc_item(w, tiles, true);
+            const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
+            // this thread's weight row (n within the expert's matrix) and validity
+            const int unit = it.tile * kTcM + m;
+            const bool row_ok = unit < p.rows;
+            const int n = b * p.rows + unit;
+            const size_t srow = ((size_t)it.e * p.N + n) * G;
+            const size_t zrow = ((size_t)it.e * (p.N / 8) + n / 8) * G;
+            const uint32_t zsh = 4u * (n & 7);
+            // this thread's four activation chunks: rows r = t/8 + 32i, chunk c = t % 8
+            const int cc = t & 7;
+            const __half *src[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = (t >> 3) + 32 * i;
+                src[i] = nullptr;
+                if (r < nrows) {
+                    const int sr = it.lo + it.chunk * kTcMaxN + r;
+                    if (MODE == kTcGateUp) {
+                        const int pr = p.sorted_pair[sr];
+                        if (pr >= 0 && pr < p.P) src[i] = p.vin + (size_t)(pr / p.k) * p.K + cc * 8;
+                    } else {
+                        src[i] = p.vin + (size_t)sr * p.K + cc * 8;
+                    }
+                }
+            }
+            // prefetched per-K-block inputs
+            uint32_t sc_n = 0, z_n[2] = {0, 0};
+            uint4 x_n[4];
+            auto fetch = [&](int kb) {
+                const int g0 = kb * 2 + (nmat == 2 ? 0 : half);
+                if (row_ok) {
+                    if (nmat == 2) {
+                        // two groups: scales g0, g0+1 (4 bytes), zero words g0, g0+1
+                        const __half *sp = p.s + srow + g0;
+                        const uint32_t lo = g0 < G ? (uint32_t)__half_as_ushort(__ldg(sp)) : 0u;
+                        const uint32_t hi = g0 + 1 < G ? (uint32_t)__half_as_ushort(__ldg(sp + 1)) : 0u;
+                        sc_n = lo | (hi << 16);
+                        z_n[0] = g0 < G ? __ldg(p.z + zrow + g0) : 0u;
+                        z_n[1] = g0 + 1 < G ? __ldg(p.z + zrow + g0 + 1) : 0u;
+                    } else {
+                        sc_n = g0 < G ? (uint32_t)__half_as_ushort(__ldg(p.s + srow + g0)) : 0u;
+                        z_n[0] = g0 < G ? __ldg(p.z + zrow + g0) : 0u;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int kk = kb * kTcKB + cc * 8;
+                    x_n[i] = (src[i] && kk < p.K) ? __ldg(reinterpret_cast<const uint4 *>(src[i] + kb * kTcKB))
+                                                   : make_uint4(0, 0, 0, 0);
+                }
+            };
+            fetch(0);
+            for (int kb = 0; kb < nkb; ++kb, ++j) {
+                const int s = j % S;
+                const uint32_t sc = sc_n, zc0 = z_n[0], zc1 = z_n[1];
+                uint4 xc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) xc[i] = x_n[i];
+                if (kb + 1 < nkb) fetch(kb + 1);
+                uint8_t *stg = smem + (size_t)Gm::stage * s;
+                // the stage's operands are free once the MMAs of its last use are done
+                if (!mbar_wait_bounded(&ctl->mma_done[s], ((j / S) & 1) ^ 1, abort_flag) ||
+                    !mbar_wait_bounded(&ctl->codes_full[s], (j / S) & 1, abort_flag)) {
+                    if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                // activation rows -> B tile (pair order, swizzled)
+                uint8_t *Bt = stg + Gm::a_bytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = (t >> 3) + 32 * i;
+                    if (r < nrows) *reinterpret_cast<uint4 *>(Bt + sw128(r, cc)) = pair_interleave(xc[i]);
+                }
+                // codes -> dequantised A tile
+                const uint8_t *codes = stg + Gm::a_bytes + Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2);
+                uint8_t *At = stg + b * (kTcM * kTcKB * 2);
+                const ZeroPoint zp0 = make_zero_point((zc0 >> zsh) & 0xFu);
+                const ZeroPoint zp1 = make_zero_point((zc1 >> zsh) & 0xFu);
+                const __half2 s0 = __half2half2(__ushort_as_half((unsigned short)(sc & 0xFFFFu)));
+                const __half2 s1 = __half2half2(__ushort_as_half((unsigned short)(sc >> 16)));
+                uint4 cw[2];
+                cw[0] = *reinterpret_cast<const uint4 *>(codes + w0 * 4);
+                if (nw == 8) cw[1] = *reinterpret_cast<const uint4 *>(codes + 16);
+#pragma unroll
+                for (int wi = 0; wi < nw; ++wi) {
+                    const uint4 &v = cw[wi >> 2];
+                    const uint32_t word = (wi & 3) == 0 ? v.x : ((wi & 3) == 1 ? v.y : ((wi & 3) == 2 ? v.z : v.w));
+                    // step 3: words 0-3 are group g0, 4-7 group g0+1; step 4: one group
+                    const bool second = nmat == 2 && wi >= 4;
+                    __half2 d[4];
+                    dequant_word(word, second ? zp1 : zp0, d);
+                    const __half2 sv = second ? s1 : s0;
+                    uint4 o;
+                    o.x = *reinterpret_cast<uint32_t *>(&(d[0] = __hmul2(d[0], sv)));
+                    o.y = *reinterpret_cast<uint32_t *>(&(d[1] = __hmul2(d[1], sv)));
+                    o.z = *reinterpret_cast<uint32_t *>(&(d[2] = __hmul2(d[2], sv)));
+                    o.w = *reinterpret_cast<uint32_t *>(&(d[3] = __hmul2(d[3], sv)));
+                    *reinterpret_cast<uint4 *>(At + sw128(m, w0 + wi)) = o;
+                }
+                fence_proxy_async();  // operands written by this thread -> tensor core reads
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->dq_done[s]);
+            }
+            w.j += gridDim.x;
+            ok = tc_load_slot(p, A, tiles, w);
+        }
+    } else {
+        // ---- epilogue: accumulators -> h (step 3) or y (step 4)
+        const int q = warp & 3;  // tensor-memory lane quadrant of this warp
+        const int m = q * 32 + lane;
+        TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
+        int n_items = 0;
+        for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag; ++n_items) {
+            const TcItem it = tc_item(w, tiles, true);
+            const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
+            const int as = n_items & 1;
+            if (!mbar_wait_bounded(&ctl->acc_full[as], (n_items >> 1) & 1, abort_flag)) {
+                if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (nmat * kTcMaxN);
+            const int unit = it.tile * kTcM + m;
+            const int r0 = it.lo + it.chunk * kTcMaxN;
+            for (int c0 = 0; c0 < nrows; c0 += 16) {
+                uint32_t g[16];
+                tc_ld16(dacc + c0, g);
+                if (MODE == kTcGateUp) {
+                    uint32_t u[16];
+                    tc_ld16(dacc + kTcMaxN + c0, u);
+                    tc_wait_ld();
+                    if (unit < p.rows) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            if (c0 + c < nrows) {
+                                const float gv = __uint_as_float(g[c]), uv = __uint_as_float(u[c]);
+                                const float hv = gv / (1.0f + __expf(-gv)) * uv;
+                                p.h_out[(size_t)(r0 + c0 + c) * p.rows + unit] = __float2half_rn(hv);
+                            }
+                        }
+                    }
+                } else {
+                    tc_wait_ld();
+                    if (unit < p.rows) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            if (c0 + c < nrows) {
+                                const int pr = __ldg(p.sorted_pair + r0 + c0 + c);
+                                if (pr >= 0 && pr < p.P) p.y_out[(size_t)pr * p.rows + unit] = __uint_as_float(g[c]);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->acc_empty[as]);
+            w.j += gridDim.x;
+            ok = tc_load_slot(p, A, tiles, w);
+        }
+    }
+
+    // ---- teardown: every role has finished; release tensor memory
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols));
+    }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+    }
+    return fn;
+}
+
+// 2-D map over the packed codes viewed as [E*N rows][K/8 words], box of
+// 8 words x 128 rows (one 64-wide K block of one tile); reads beyond the
+// tensor return zeros.
+cudaError_t codes_map(CUtensorMap *map, const uint32_t *q, int E, int N, int K) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)(K / 8), (cuuint64_t)E * N};
+    const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
+    const cuuint32_t box[2] = {kTcKB / 8, kTcM};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(q), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, int num_sms, size_t smem_limit, cudaStream_t stream) {
+    using Gm = TcGeom<MODE>;
+    TcArgs a = a0;
+    int S = (int)((smem_limit - 1024 - sizeof(TcCtrl)) / Gm::stage);
+    if (S < 2) return cudaErrorInvalidConfiguration;
+    a.nstages = S > kTcMaxStages ? kTcMaxStages : S;
+    const size_t smem = tc_smem_bytes(Gm::stage, a.nstages);
+    CUtensorMap map;
+    cudaError_t e = codes_map(&map, q, a.E, a.N, a.K);
+    if (e != cudaSuccess) return e;
+    static int configured[128];
+    e = ensure_smem(tc_kernel<MODE>, configured, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(tc_kernel<MODE>, num_sms, kTcThreads, smem, stream, a, map);
+}
+
+}  // namespace
+
+// Shapes the tensor-core path takes: fp16 activations with K a multiple of
+// 32 (groups) and enough rows per expert on average to fill MMA granules.
+bool tc_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
+    (void)E;
+    (void)k;
+    return T >= kTcMinT && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
+           tc_smem_bytes(TcGeom<kTcGateUp>::stage, 2) <= smem_limit;
+}
+
+cudaError_t launch_gate_up_tc(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
+                              const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
+                              const int32_t *num_active, int T, int E, int k, int H, int I, __half *h, uint32_t *err,
+                              int num_sms, size_t smem_limit, cudaStream_t stream) {
+    TcArgs a{};
+    a.s = s; a.z = z; a.vin = x;
+    a.E = E; a.N = 2 * I; a.K = H; a.rows = I;
+    a.T = T; a.k = k; a.P = T * k;
+    a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
+    a.h_out = h; a.err = err;
+    return launch_tc<kTcGateUp>(a, q, num_sms, smem_limit, stream);
+}
+
+cudaError_t launch_combine(const float *y, const float *topk_w, int T, int k, int H, __half *out,
+                           cudaStream_t stream);
+
+cudaError_t launch_down_tc(const __half *h, const uint32_t *q, const __half *s, const uint32_t *z,
+                           const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
+                           const int32_t *num_active, const float *topk_w, int T, int E, int k, int H, int I,
+                           __half *out, float *y, uint32_t *err, int num_sms, size_t smem_limit,
+                           cudaStream_t stream) {
+    TcArgs a{};
+    a.s = s; a.z = z; a.vin = h;
+    a.E = E; a.N = H; a.K = I; a.rows = H;
+    a.T = T; a.k = k; a.P = T * k;
+    a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
+    a.y_out = y; a.err = err;
+    cudaError_t e = launch_tc<kTcDown>(a, q, num_sms, smem_limit, stream);
+    if (e != cudaSuccess) return e;
+    return launch_combine(y, topk_w, T, k, H, out, stream);
+}
+
+}  // namespace moe

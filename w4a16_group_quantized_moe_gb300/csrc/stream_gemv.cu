@@ -437,6 +437,12 @@ __global__ void combine_kernel(const float *__restrict__ y, const float *__restr
     reinterpret_cast<uint4 *>(out + (size_t)t * H)[nb] = o;
 }
 
+cudaError_t launch_combine(const float *y, const float *topk_w, int T, int k, int H, __half *out,
+                           cudaStream_t stream) {
+    const long long n = (long long)T * (H / 8);
+    return launch_pdl(combine_kernel, (unsigned)((n + 255) / 256), 256, 0, stream, y, topk_w, T, k, H, out);
+}
+
 // ---------------------------------------------------------------- launchers
 template <int MODE, int S>
 static cudaError_t launch_stream_t(StreamArgs a, int num_sms, size_t smem_limit, cudaStream_t stream) {
