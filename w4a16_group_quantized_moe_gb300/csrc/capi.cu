@@ -37,7 +37,7 @@ cudaError_t launch_down_decode(const __half *, const uint32_t *, const __half *,
 bool tc_supported(int, int, int, int, int, size_t);
 cudaError_t launch_gate_up_tc(const __half *, const uint32_t *, const __half *, const uint32_t *,
                               const int32_t *, const int32_t *, const int32_t *, const int32_t *, int, int,
-                              int, int, int, __half *, uint32_t *, int, size_t, cudaStream_t);
+                              int, int, int, __half *, __half *, uint32_t *, int, size_t, cudaStream_t);
 cudaError_t launch_down_tc(const __half *, const uint32_t *, const __half *, const uint32_t *,
                            const int32_t *, const int32_t *, const int32_t *, const int32_t *, const float *,
                            int, int, int, int, int, __half *, float *, uint32_t *, int, size_t, cudaStream_t);
@@ -232,7 +232,10 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
         return cuda_status(launch_gate_up_tc(
             reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,
             expert_offsets, sorted_pair, active_experts, num_active, T, E, k, H, I,
-            reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
+            reinterpret_cast<__half *>(h),
+            // scratch for the sorted x rows: the per-pair y area, unused until step 4
+            reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + workspace_layout(T, k, H).y), err,
+            di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
     e = launch_gate_up_stream(reinterpret_cast<const __half *>(x), w13_q,
                               reinterpret_cast<const __half *>(w13_s), w13_z, expert_offsets,
                               sorted_pair, active_experts, num_active, T, E, k, H, I,

@@ -12,25 +12,31 @@
 // beyond one 16-row MMA granule.
 //
 // One persistent CTA per SM, warp-specialised, all stages in shared memory:
-//   warp 0      bulk tensor copies (TMA) of the packed codes of each 64-wide
-//               K block (gate and up tiles, or the down tile)
+//   warp 0      bulk tensor copies (TMA) per 64-wide K block, into a ring
+//               of copy stages: the packed codes of the tile(s), and the
+//               chunk's activation rows in the 128-byte-swizzled K-major
+//               operand layout, one copy (step 3 reads a sorted,
+//               pair-ordered copy of the x rows made by sorted_rows_kernel;
+//               step 4 the h rows, already in sorted order)
 //   warps 2-9   dequantise the codes to fp16 ((q - z) * s, per 32-wide
-//               group, exact q - z from the binary16 exponent trick) into
-//               the 128-byte-swizzled K-major operand layout, and gather the
-//               activation rows of the chunk into the same layout (both in
-//               the pair order [k0 k4 k1 k5 k2 k6 k3 k7] of the dequantiser:
-//               the contraction over K does not depend on the order)
+//               group, exact q - z from the binary16 exponent trick) into the
+//               same layout; step 3 keeps the dequantiser's pair order
+//               [k0 k4 k1 k5 k2 k6 k3 k7] (x was permuted alike: the
+//               contraction over K does not depend on the order), step 4
+//               restores natural order to match h
 //   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate in
 //               tensor memory) for each K block and commits to mbarriers
 //   warps 10-13 read the accumulators (tcgen05.ld) and finish: h =
 //               silu(gate) * up in fp16 (step 3), or the fp32 per-pair
 //               projection y (step 4, summed per token by combine_kernel)
-// Stages rotate through a ring (codes -> dequantised operands -> MMA) and
-// the accumulators are double-buffered, so dequantisation, MMA and the
-// epilogue of consecutive tiles overlap.  Every wait is bounded.
+// The copy ring is as deep as shared memory allows (it covers the HBM
+// latency of the codes), the dequantised tiles have their own two-stage
+// ring, and the accumulators are double-buffered, so copies,
+// dequantisation, MMA and the epilogue of consecutive tiles overlap.
+// Every wait is bounded.
 #include <cuda.h>
 
-#include "common.cuh"
+#include "align.cuh"
 
 namespace moe {
 
@@ -40,7 +46,8 @@ constexpr int kTcEpiWarp0 = 10, kTcEpiWarps = 4;
 constexpr int kTcM = 128;     // weight rows per tile
 constexpr int kTcKB = 64;     // K per stage: one 128-byte row of fp16
 constexpr int kTcMaxN = 128;  // activation rows per chunk
-constexpr int kTcMaxStages = 6;
+constexpr int kTcMaxStages = 8;   // copy ring
+constexpr int kTcMaxAStages = 4;  // dequantised-tile ring
 constexpr int kTcMinT = 64;   // smaller batches stay on the CUDA-core stream kernels
 constexpr uint32_t kTcTmemCols = 512;
 
@@ -59,23 +66,28 @@ struct TcArgs {
     __half *h_out;      // step 3: [P][I]
     float *y_out;       // step 4: [P][H]
     uint32_t *err;
-    int nstages;
+    int nstages, astages;
+    int amax;  // slot table capacity: min(E, P)
 };
 
 template <int MODE>
 struct TcGeom {
     static constexpr int nmat = MODE == kTcGateUp ? 2 : 1;
-    static constexpr uint32_t a_bytes = nmat * kTcM * kTcKB * 2;  // dequantised tiles
-    static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows
-    static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes
-    static constexpr uint32_t stage = a_bytes + b_bytes + c_bytes;  // multiple of 1024
+    static constexpr uint32_t a_bytes = nmat * kTcM * kTcKB * 2;  // dequantised tile(s): the A ring
+    static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows   } the copy
+    static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes      } ring
+    static constexpr uint32_t t_bytes = b_bytes + c_bytes;        // multiples of 1024
 };
 
-// Control block after the stages: mbarriers and the tensor-memory address.
+// Control block after the rings: mbarriers and the tensor-memory address.
+//   t_full/t_free: copy ring (codes and activation rows of a K block)
+//   a_full/a_free: dequantised A tiles (astages stages)
+//   acc_full/acc_empty: the two accumulator buffers in tensor memory
 struct TcCtrl {
-    uint64_t codes_full[kTcMaxStages];
-    uint64_t dq_done[kTcMaxStages];
-    uint64_t mma_done[kTcMaxStages];
+    uint64_t t_full[kTcMaxStages];
+    uint64_t t_free[kTcMaxStages];
+    uint64_t a_full[kTcMaxAStages];
+    uint64_t a_free[kTcMaxAStages];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -83,8 +95,8 @@ struct TcCtrl {
     int abort;
 };
 
-__host__ __device__ inline size_t tc_smem_bytes(uint32_t stage, int nstages) {
-    return 1024 + (size_t)stage * nstages + sizeof(TcCtrl);
+__host__ __device__ inline size_t tc_smem_bytes(uint32_t a_bytes, int astages, uint32_t t_bytes, int nstages) {
+    return 1024 + (size_t)a_bytes * astages + (size_t)t_bytes * nstages + sizeof(TcCtrl);
 }
 
 // ---------------------------------------------------------------- PTX
@@ -143,55 +155,52 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 
 // ---------------------------------------------------------------- work list
 // Work items, in order: for each active slot a, for each chunk of up to
-// kTcMaxN segment rows, for each 128-row weight tile.  A cursor walks them
-// with a stride (the grid), reading the routing metadata from global memory.
+// kTcMaxN segment rows, for each 128-row weight tile.  Each CTA builds the
+// table of slots (expert, first sorted row, rows, first item) in shared
+// memory once; item i of the grid-strided sequence is found by binary
+// search over the first-item prefix.
 struct TcItem {
     int a, e, lo, ne, tile, chunk;  // slot, expert, first sorted row, segment rows, tile, chunk
-    bool valid;
 };
 
-struct TcWalk {
-    int a, j;        // slot and item index within the slot
-    int nitems;      // items of slot a
-    int e, lo, ne;
+struct TcTable {
+    int *e, *lo, *ne, *pre;  // pre: [A+1] first item of each slot
 };
 
-__device__ __forceinline__ bool tc_load_slot(const TcArgs &p, int A, int tiles, TcWalk &w) {
-    while (w.a < A) {
-        w.e = p.active[w.a];
-        if (w.e < 0 || w.e >= p.E) return false;
-        w.lo = p.offsets[w.e];
-        w.ne = p.offsets[w.e + 1] - w.lo;
-        w.nitems = tiles * ((w.ne + kTcMaxN - 1) / kTcMaxN);
-        if (w.j < w.nitems) return true;
-        w.j -= w.nitems;
-        ++w.a;
+__device__ __forceinline__ TcItem tc_lookup(const TcTable &tb, int A, int tiles, int i) {
+    int lo = 0, hi = A;  // pre[lo] <= i < pre[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tb.pre[mid] <= i) lo = mid; else hi = mid;
     }
-    return false;
-}
-
-__device__ __forceinline__ TcItem tc_item(const TcWalk &w, int tiles, bool ok) {
     TcItem it;
-    it.valid = ok;
-    it.a = w.a;
-    it.e = w.e;
-    it.lo = w.lo;
-    it.ne = w.ne;
-    it.chunk = w.j / tiles;
-    it.tile = w.j - it.chunk * tiles;
+    it.a = lo;
+    it.e = tb.e[lo];
+    it.lo = tb.lo[lo];
+    it.ne = tb.ne[lo];
+    const int j = i - tb.pre[lo];
+    it.chunk = j / tiles;
+    it.tile = j - it.chunk * tiles;
     return it;
 }
+
+__host__ __device__ inline size_t tc_table_bytes(int amax) { return ((size_t)5 * amax + 1 + 128) * 4; }
 
 // ---------------------------------------------------------------- kernel
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap qmap) {
+    tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap bmap) {
     using Gm = TcGeom<MODE>;
     constexpr int nmat = Gm::nmat;
     extern __shared__ uint8_t tc_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int S = p.nstages;
-    TcCtrl *ctl = reinterpret_cast<TcCtrl *>(smem + (size_t)Gm::stage * S);
+    const int S = p.nstages, SA = p.astages;
+    uint8_t *aring = smem;                             // [SA][a_bytes]
+    uint8_t *tring = smem + (size_t)SA * Gm::a_bytes;  // [S][b_bytes + c_bytes]
+    TcCtrl *ctl = reinterpret_cast<TcCtrl *>(tring + (size_t)Gm::t_bytes * S);
+    int *tbase = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ctl) + align_up(sizeof(TcCtrl), 16));
+    const TcTable tb{tbase, tbase + p.amax, tbase + 2 * p.amax, tbase + 3 * p.amax};
+    int *t_tmp = tbase + 4 * p.amax + 1, *t_scratch = t_tmp + p.amax;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.K / 32;
     const int nkb = (p.K + kTcKB - 1) / kTcKB;
@@ -199,9 +208,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&ctl->codes_full[s], 1);
-            mbar_init(&ctl->dq_done[s], kTcDqWarps);
-            mbar_init(&ctl->mma_done[s], 1);
+            mbar_init(&ctl->t_full[s], 1);
+            mbar_init(&ctl->t_free[s], 1);
+        }
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(&ctl->a_full[s], kTcDqWarps);
+            mbar_init(&ctl->a_free[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&ctl->acc_full[s], 1);
@@ -225,54 +237,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_trigger();
 
     int A = *p.num_active;
-    A = A < 0 ? 0 : (A > p.E ? p.E : A);
+    A = A < 0 ? 0 : (A > p.amax ? p.amax : A);
     auto fail = [&](uint32_t bits) {
         set_error(p.err, bits);
         *abort_flag = 1;
     };
+    // slot table: expert, segment, items (tiles x chunks), then their prefix
+    for (int a = tid; a < A; a += kTcThreads) {
+        const int e = p.active[a];
+        int lo = 0, ne = 0;
+        if (e >= 0 && e < p.E) {
+            lo = p.offsets[e];
+            ne = p.offsets[e + 1] - lo;
+        }
+        if (ne < 0 || lo < 0 || lo + ne > p.P) ne = 0;
+        tb.e[a] = e;
+        tb.lo[a] = lo;
+        tb.ne[a] = ne;
+        tb.pre[a] = tiles * ((ne + kTcMaxN - 1) / kTcMaxN);
+        t_tmp[a] = 0;
+    }
+    __syncthreads();
+    const int n_items = block_exclusive_scan2(tb.pre, t_tmp, A, t_scratch).x;
+    if (tid == 0) tb.pre[A] = n_items;
+    __syncthreads();
 
     if (warp == kTcProducerWarp) {
-        // ---- codes of every K block of every item, through the ring
-        if (lane == 0) {
-            TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
-            int j = 0;  // stage counter
-            for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag;) {
-                const TcItem it = tc_item(w, tiles, true);
-                for (int kb = 0; kb < nkb; ++kb, ++j) {
-                    const int s = j % S;
-                    if (!mbar_wait_bounded(&ctl->dq_done[s], ((j / S) & 1) ^ 1, abort_flag)) {
-                        if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
-                        break;
-                    }
-                    uint8_t *codes = smem + (size_t)Gm::stage * s + Gm::a_bytes + Gm::b_bytes;
-                    mbar_arrive_expect_tx(&ctl->codes_full[s], Gm::c_bytes);
+        // ---- codes and activation rows of every K block, through the copy ring
+        int j = 0;
+        for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
+            const TcItem it = tc_lookup(tb, A, tiles, ii);
+            const int r0 = it.lo + it.chunk * kTcMaxN;
+            for (int kb = 0; kb < nkb; ++kb, ++j) {
+                const int s = j % S;
+                // the stage is free once the MMAs of its last use are done
+                // (every lane waits; the decision is made warp-uniform)
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ctl->t_free[s], ((j / S) & 1) ^ 1, abort_flag))) {
+                    if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                if (lane == 0) {
+                    uint8_t *stg = tring + (size_t)Gm::t_bytes * s;
+                    mbar_arrive_expect_tx(&ctl->t_full[s], Gm::t_bytes);
 #pragma unroll
                     for (int b = 0; b < nmat; ++b) {
                         const int row = it.e * p.N + b * p.rows + it.tile * kTcM;
-                        tma_load_2d(codes + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row, &ctl->codes_full[s]);
+                        tma_load_2d(stg + Gm::b_bytes + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row,
+                                    &ctl->t_full[s]);
                     }
+                    tma_load_2d(stg, &bmap, kb * kTcKB, r0, &ctl->t_full[s]);
                 }
-                w.j += gridDim.x;
-                ok = tc_load_slot(p, A, tiles, w);
+                __syncwarp();
             }
-            if (*abort_flag) {
-                // never leave with a copy in flight: wait for the last issue of each stage
-                for (int jj = j > S ? j - S : 0; jj < j; ++jj)
-                    mbar_wait_bounded(&ctl->codes_full[jj % S], (jj / S) & 1, nullptr);
-            }
+        }
+        if (lane == 0 && *abort_flag) {
+            // never leave with a copy in flight: wait for the last issue of each stage
+            for (int jj = j > S ? j - S : 0; jj < j; ++jj)
+                mbar_wait_bounded(&ctl->t_full[jj % S], (jj / S) & 1, nullptr);
         }
     } else if (warp == kTcMmaWarp) {
         // ---- one thread issues the MMAs
         if (lane == 0) {
-            TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
-            int j = 0, n_items = 0;
-            for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag; ++n_items) {
-                const TcItem it = tc_item(w, tiles, true);
+            int j = 0, n_done = 0;
+            for (int ii = blockIdx.x; ii < n_items && !*abort_flag; ii += gridDim.x, ++n_done) {
+                const TcItem it = tc_lookup(tb, A, tiles, ii);
                 const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
-                const int nmma = (nrows + 15) & ~15;
-                const uint32_t idesc = tc_idesc(nmma);
-                const int as = n_items & 1;
-                if (!mbar_wait_bounded(&ctl->acc_empty[as], ((n_items >> 1) & 1) ^ 1, abort_flag)) {
+                const uint32_t idesc = tc_idesc((nrows + 15) & ~15);
+                const int as = n_done & 1;
+                if (!mbar_wait_bounded(&ctl->acc_empty[as], ((n_done >> 1) & 1) ^ 1, abort_flag)) {
                     if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -280,131 +312,100 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t dacc = tmem + (uint32_t)as * (nmat * kTcMaxN);
                 bool broke = false;
                 for (int kb = 0; kb < nkb; ++kb, ++j) {
-                    const int s = j % S;
-                    if (!mbar_wait_bounded(&ctl->dq_done[s], (j / S) & 1, abort_flag)) {
+                    const int s = j % S, s2 = j % SA;
+                    if (!mbar_wait_bounded(&ctl->a_full[s2], (j / SA) & 1, abort_flag) ||
+                        !mbar_wait_bounded(&ctl->t_full[s], (j / S) & 1, abort_flag)) {
                         if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                         broke = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sbase = smem_addr(smem + (size_t)Gm::stage * s);
+                    const uint32_t abase = smem_addr(aring + (size_t)Gm::a_bytes * s2);
+                    const uint32_t bbase = smem_addr(tring + (size_t)Gm::t_bytes * s);
 #pragma unroll
                     for (int ks = 0; ks < kTcKB / 16; ++ks) {
-                        const uint64_t bd = tc_desc_sw128(sbase + Gm::a_bytes + ks * 32);
+                        const uint64_t bd = tc_desc_sw128(bbase + ks * 32);
 #pragma unroll
                         for (int b = 0; b < nmat; ++b) {
-                            const uint64_t ad = tc_desc_sw128(sbase + b * (kTcM * kTcKB * 2) + ks * 32);
+                            const uint64_t ad = tc_desc_sw128(abase + b * (kTcM * kTcKB * 2) + ks * 32);
                             tc_mma(dacc + b * kTcMaxN, ad, bd, idesc, (kb | ks) != 0);
                         }
                     }
-                    tc_commit(&ctl->mma_done[s]);
+                    tc_commit(&ctl->t_free[s]);
+                    tc_commit(&ctl->a_free[s2]);
                 }
                 if (broke) break;
                 tc_commit(&ctl->acc_full[as]);
-                w.j += gridDim.x;
-                ok = tc_load_slot(p, A, tiles, w);
             }
             // every MMA this thread issued has completed before tensor memory is released
             tc_commit(&ctl->drain);
             mbar_wait_bounded(&ctl->drain, 0, nullptr);
         }
     } else if (warp >= kTcDqWarp0 && warp < kTcDqWarp0 + kTcDqWarps) {
-        // ---- dequantise the codes and gather the activation rows
+        // ---- dequantise the codes into the A tile(s)
         const int t = tid - kTcDqWarp0 * 32;  // 0..255
-        // A rows: step 3: matrix b = t / 128, row m = t % 128, all 8 words;
-        // step 4: row m = t % 128, words [4h, 4h+4) with h = t / 128
+        // step 3: matrix b = t / 128, row m = t % 128, all 8 words of the K
+        // block; step 4: row m = t % 128, words [4h, 4h+4) with h = t / 128
         const int m = t & 127, half = t >> 7;
         const int b = nmat == 2 ? half : 0;
-        const int w0 = nmat == 2 ? 0 : 4 * half, nw = nmat == 2 ? 8 : 4;
-        TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
+        const int w0 = nmat == 2 ? 0 : 4 * half;
         int j = 0;
-        for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag;) {
-            const TcItem it = tc_item(w, tiles, true);
-            const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
-            // this thread's weight row (n within the expert's matrix) and validity
+        for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
+            const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int unit = it.tile * kTcM + m;
             const bool row_ok = unit < p.rows;
             const int n = b * p.rows + unit;
             const size_t srow = ((size_t)it.e * p.N + n) * G;
             const size_t zrow = ((size_t)it.e * (p.N / 8) + n / 8) * G;
             const uint32_t zsh = 4u * (n & 7);
-            // this thread's four activation chunks: rows r = t/8 + 32i, chunk c = t % 8
-            const int cc = t & 7;
-            const __half *src[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = (t >> 3) + 32 * i;
-                src[i] = nullptr;
-                if (r < nrows) {
-                    const int sr = it.lo + it.chunk * kTcMaxN + r;
-                    if (MODE == kTcGateUp) {
-                        const int pr = p.sorted_pair[sr];
-                        if (pr >= 0 && pr < p.P) src[i] = p.vin + (size_t)(pr / p.k) * p.K + cc * 8;
-                    } else {
-                        src[i] = p.vin + (size_t)sr * p.K + cc * 8;
-                    }
-                }
-            }
-            // prefetched per-K-block inputs
-            uint32_t sc_n = 0, z_n[2] = {0, 0};
-            uint4 x_n[4];
-            auto fetch = [&](int kb) {
+            // scales and zero words, fetched three K blocks ahead: (scale
+            // pair, zero word of the first group, zero word of the second)
+            uint32_t f0[3] = {0, 0, 0}, f1[3] = {0, 0, 0}, f2[3] = {0, 0, 0};
+            auto fetch = [&](int kb, uint32_t (&f)[3]) {
+                f[0] = f[1] = f[2] = 0;
+                if (!row_ok || kb >= nkb) return;
                 const int g0 = kb * 2 + (nmat == 2 ? 0 : half);
-                if (row_ok) {
-                    if (nmat == 2) {
-                        // two groups: scales g0, g0+1 (4 bytes), zero words g0, g0+1
-                        const __half *sp = p.s + srow + g0;
-                        const uint32_t lo = g0 < G ? (uint32_t)__half_as_ushort(__ldg(sp)) : 0u;
-                        const uint32_t hi = g0 + 1 < G ? (uint32_t)__half_as_ushort(__ldg(sp + 1)) : 0u;
-                        sc_n = lo | (hi << 16);
-                        z_n[0] = g0 < G ? __ldg(p.z + zrow + g0) : 0u;
-                        z_n[1] = g0 + 1 < G ? __ldg(p.z + zrow + g0 + 1) : 0u;
-                    } else {
-                        sc_n = g0 < G ? (uint32_t)__half_as_ushort(__ldg(p.s + srow + g0)) : 0u;
-                        z_n[0] = g0 < G ? __ldg(p.z + zrow + g0) : 0u;
-                    }
+                if (g0 < G) {
+                    f[0] = (uint32_t)__half_as_ushort(__ldg(p.s + srow + g0));
+                    f[1] = __ldg(p.z + zrow + g0);
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int kk = kb * kTcKB + cc * 8;
-                    x_n[i] = (src[i] && kk < p.K) ? __ldg(reinterpret_cast<const uint4 *>(src[i] + kb * kTcKB))
-                                                   : make_uint4(0, 0, 0, 0);
+                if (nmat == 2 && g0 + 1 < G) {
+                    f[0] |= (uint32_t)__half_as_ushort(__ldg(p.s + srow + g0 + 1)) << 16;
+                    f[2] = __ldg(p.z + zrow + g0 + 1);
                 }
             };
-            fetch(0);
+            fetch(0, f0);
+            fetch(1, f1);
+            fetch(2, f2);
             for (int kb = 0; kb < nkb; ++kb, ++j) {
-                const int s = j % S;
-                const uint32_t sc = sc_n, zc0 = z_n[0], zc1 = z_n[1];
-                uint4 xc[4];
+                const int s = j % S, s2 = j % SA;
+                const uint32_t sc = f0[0], zc0 = f0[1], zc1 = f0[2];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) xc[i] = x_n[i];
-                if (kb + 1 < nkb) fetch(kb + 1);
-                uint8_t *stg = smem + (size_t)Gm::stage * s;
-                // the stage's operands are free once the MMAs of its last use are done
-                if (!mbar_wait_bounded(&ctl->mma_done[s], ((j / S) & 1) ^ 1, abort_flag) ||
-                    !mbar_wait_bounded(&ctl->codes_full[s], (j / S) & 1, abort_flag)) {
-                    if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+                for (int i = 0; i < 3; ++i) {
+                    f0[i] = f1[i];
+                    f1[i] = f2[i];
+                }
+                fetch(kb + 3, f2);
+                // the codes of this K block have landed; the A stage is free
+                // once the MMAs of its last use are done
+                const bool w_ok = mbar_wait_bounded(&ctl->t_full[s], (j / S) & 1, abort_flag) &&
+                                  mbar_wait_bounded(&ctl->a_free[s2], ((j / SA) & 1) ^ 1, abort_flag);
+                if (!__all_sync(0xffffffffu, w_ok)) {
+                    if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                // activation rows -> B tile (pair order, swizzled)
-                uint8_t *Bt = stg + Gm::a_bytes;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = (t >> 3) + 32 * i;
-                    if (r < nrows) *reinterpret_cast<uint4 *>(Bt + sw128(r, cc)) = pair_interleave(xc[i]);
-                }
-                // codes -> dequantised A tile
-                const uint8_t *codes = stg + Gm::a_bytes + Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2);
-                uint8_t *At = stg + b * (kTcM * kTcKB * 2);
+                const uint8_t *codes =
+                    tring + (size_t)Gm::t_bytes * s + Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2);
+                uint8_t *At = aring + (size_t)Gm::a_bytes * s2 + b * (kTcM * kTcKB * 2);
                 const ZeroPoint zp0 = make_zero_point((zc0 >> zsh) & 0xFu);
                 const ZeroPoint zp1 = make_zero_point((zc1 >> zsh) & 0xFu);
                 const __half2 s0 = __half2half2(__ushort_as_half((unsigned short)(sc & 0xFFFFu)));
                 const __half2 s1 = __half2half2(__ushort_as_half((unsigned short)(sc >> 16)));
                 uint4 cw[2];
                 cw[0] = *reinterpret_cast<const uint4 *>(codes + w0 * 4);
-                if (nw == 8) cw[1] = *reinterpret_cast<const uint4 *>(codes + 16);
+                if (nmat == 2) cw[1] = *reinterpret_cast<const uint4 *>(codes + 16);
 #pragma unroll
-                for (int wi = 0; wi < nw; ++wi) {
+                for (int wi = 0; wi < (nmat == 2 ? 8 : 4); ++wi) {
                     const uint4 &v = cw[wi >> 2];
                     const uint32_t word = (wi & 3) == 0 ? v.x : ((wi & 3) == 1 ? v.y : ((wi & 3) == 2 ? v.z : v.w));
                     // step 3: words 0-3 are group g0, 4-7 group g0+1; step 4: one group
@@ -412,38 +413,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     __half2 d[4];
                     dequant_word(word, second ? zp1 : zp0, d);
                     const __half2 sv = second ? s1 : s0;
+                    uint32_t u[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __half2 v2 = __hmul2(d[i], sv);
+                        u[i] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
                     uint4 o;
-                    o.x = *reinterpret_cast<uint32_t *>(&(d[0] = __hmul2(d[0], sv)));
-                    o.y = *reinterpret_cast<uint32_t *>(&(d[1] = __hmul2(d[1], sv)));
-                    o.z = *reinterpret_cast<uint32_t *>(&(d[2] = __hmul2(d[2], sv)));
-                    o.w = *reinterpret_cast<uint32_t *>(&(d[3] = __hmul2(d[3], sv)));
+                    if (MODE == kTcGateUp) {
+                        o = make_uint4(u[0], u[1], u[2], u[3]);  // pair order, like the sorted x copy
+                    } else {
+                        // natural order: (k0,k1) (k2,k3) (k4,k5) (k6,k7)
+                        o.x = __byte_perm(u[0], u[1], 0x5410);
+                        o.y = __byte_perm(u[2], u[3], 0x5410);
+                        o.z = __byte_perm(u[0], u[1], 0x7632);
+                        o.w = __byte_perm(u[2], u[3], 0x7632);
+                    }
                     *reinterpret_cast<uint4 *>(At + sw128(m, w0 + wi)) = o;
                 }
                 fence_proxy_async();  // operands written by this thread -> tensor core reads
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->dq_done[s]);
+                if (lane == 0) mbar_arrive(&ctl->a_full[s2]);
             }
-            w.j += gridDim.x;
-            ok = tc_load_slot(p, A, tiles, w);
         }
     } else {
         // ---- epilogue: accumulators -> h (step 3) or y (step 4)
         const int q = warp & 3;  // tensor-memory lane quadrant of this warp
         const int m = q * 32 + lane;
-        TcWalk w{0, (int)blockIdx.x, 0, 0, 0, 0};
-        int n_items = 0;
-        for (bool ok = tc_load_slot(p, A, tiles, w); ok && !*abort_flag; ++n_items) {
-            const TcItem it = tc_item(w, tiles, true);
+        int n_done = 0;
+        for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x, ++n_done) {
+            const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
-            const int as = n_items & 1;
-            if (!mbar_wait_bounded(&ctl->acc_full[as], (n_items >> 1) & 1, abort_flag)) {
-                if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
+            const int as = n_done & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ctl->acc_full[as], (n_done >> 1) & 1, abort_flag))) {
+                if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                 break;
             }
             tc_fence_after();
             const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (nmat * kTcMaxN);
             const int unit = it.tile * kTcM + m;
             const int r0 = it.lo + it.chunk * kTcMaxN;
+            // step 4: pair ids of the chunk's rows, lane l holding rows l + 32i
+            int prs[4] = {-1, -1, -1, -1};
+            if (MODE == kTcDown) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (lane + 32 * i < nrows) prs[i] = __ldg(p.sorted_pair + r0 + lane + 32 * i);
+            }
             for (int c0 = 0; c0 < nrows; c0 += 16) {
                 uint32_t g[16];
                 tc_ld16(dacc + c0, g);
@@ -463,22 +479,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 } else {
                     tc_wait_ld();
-                    if (unit < p.rows) {
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            if (c0 + c < nrows) {
-                                const int pr = __ldg(p.sorted_pair + r0 + c0 + c);
-                                if (pr >= 0 && pr < p.P) p.y_out[(size_t)pr * p.rows + unit] = __uint_as_float(g[c]);
-                            }
-                        }
+                    for (int c = 0; c < 16; ++c) {
+                        // every lane takes part in the shuffle; only valid rows store
+                        const int col = c0 + c, q4 = col >> 5;
+                        const int v = q4 == 0 ? prs[0] : (q4 == 1 ? prs[1] : (q4 == 2 ? prs[2] : prs[3]));
+                        const int pr = __shfl_sync(0xffffffffu, v, col & 31);
+                        if (unit < p.rows && col < nrows && pr >= 0 && pr < p.P)
+                            p.y_out[(size_t)pr * p.rows + unit] = __uint_as_float(g[c]);
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->acc_empty[as]);
-            w.j += gridDim.x;
-            ok = tc_load_slot(p, A, tiles, w);
         }
     }
 
@@ -529,21 +543,64 @@ cudaError_t codes_map(CUtensorMap *map, const uint32_t *q, int E, int N, int K) 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2-D map over fp16 activation rows [rows][K] with the 128-byte swizzle;
+// box of 64 elements x box_rows rows.
+cudaError_t rows_map(CUtensorMap *map, const __half *base, long long rows, int K, int box_rows) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {kTcKB, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int MODE>
-cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, int num_sms, size_t smem_limit, cudaStream_t stream) {
+cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, const __half *brows, long long nbrows, int num_sms,
+                      size_t smem_limit, cudaStream_t stream) {
     using Gm = TcGeom<MODE>;
     TcArgs a = a0;
-    int S = (int)((smem_limit - 1024 - sizeof(TcCtrl)) / Gm::stage);
-    if (S < 2) return cudaErrorInvalidConfiguration;
+    a.amax = a.E < a.P ? a.E : a.P;
+    // the deepest A ring (up to 4) that leaves at least 4 copy stages
+    const size_t base = tc_smem_bytes(0, 0, 0, 0) + 16 + tc_table_bytes(a.amax);
+    a.astages = 0;
+    for (int sa = kTcMaxAStages; sa >= 2; --sa)
+        if (base + (size_t)sa * Gm::a_bytes + 4 * (size_t)Gm::t_bytes <= smem_limit) {
+            a.astages = sa;
+            break;
+        }
+    if (a.astages == 0) return cudaErrorInvalidConfiguration;
+    const size_t fixed = base + (size_t)a.astages * Gm::a_bytes;
+    const int S = (int)((smem_limit - fixed) / Gm::t_bytes);
     a.nstages = S > kTcMaxStages ? kTcMaxStages : S;
-    const size_t smem = tc_smem_bytes(Gm::stage, a.nstages);
-    CUtensorMap map;
+    const size_t smem = fixed + (size_t)Gm::t_bytes * a.nstages;
+    CUtensorMap map, bmap;
     cudaError_t e = codes_map(&map, q, a.E, a.N, a.K);
+    if (e != cudaSuccess) return e;
+    e = rows_map(&bmap, brows, nbrows, a.K, kTcMaxN);
     if (e != cudaSuccess) return e;
     static int configured[128];
     e = ensure_smem(tc_kernel<MODE>, configured, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(tc_kernel<MODE>, num_sms, kTcThreads, smem, stream, a, map);
+    return launch_pdl(tc_kernel<MODE>, num_sms, kTcThreads, smem, stream, a, map, bmap);
+}
+
+// xs[r] = x[token of sorted row r], each 8-element block in the
+// dequantiser's pair order (rows of invalid pairs: zeros).  Step 3 then
+// reads the activation rows of a chunk as one contiguous tile.
+__global__ void sorted_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ sorted_pair, int k,
+                                   int P, int H8, uint4 *__restrict__ xs) {
+    pdl_wait();
+    pdl_trigger();
+    const long long n = (long long)P * H8;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / H8), c = (int)(i - (long long)r * H8);
+        const int pr = __ldg(sorted_pair + r);
+        xs[i] = (pr >= 0 && pr < P) ? pair_interleave(__ldg(x + (size_t)(pr / k) * H8 + c)) : make_uint4(0, 0, 0, 0);
+    }
 }
 
 }  // namespace
@@ -551,23 +608,27 @@ cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, int num_sms, size_t s
 // Shapes the tensor-core path takes: fp16 activations with K a multiple of
 // 32 (groups) and enough rows per expert on average to fill MMA granules.
 bool tc_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
-    (void)E;
-    (void)k;
+    const int amax = E < T * k ? E : T * k;
     return T >= kTcMinT && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
-           tc_smem_bytes(TcGeom<kTcGateUp>::stage, 2) <= smem_limit;
+           tc_smem_bytes(TcGeom<kTcGateUp>::a_bytes, 2, TcGeom<kTcGateUp>::t_bytes, 4) + 16 + tc_table_bytes(amax) <=
+               smem_limit;
 }
 
 cudaError_t launch_gate_up_tc(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
                               const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
-                              const int32_t *num_active, int T, int E, int k, int H, int I, __half *h, uint32_t *err,
-                              int num_sms, size_t smem_limit, cudaStream_t stream) {
+                              const int32_t *num_active, int T, int E, int k, int H, int I, __half *h, __half *xperm,
+                              uint32_t *err, int num_sms, size_t smem_limit, cudaStream_t stream) {
     TcArgs a{};
     a.s = s; a.z = z; a.vin = x;
     a.E = E; a.N = 2 * I; a.K = H; a.rows = I;
     a.T = T; a.k = k; a.P = T * k;
     a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
     a.h_out = h; a.err = err;
-    return launch_tc<kTcGateUp>(a, q, num_sms, smem_limit, stream);
+    // the sorted, pair-ordered x rows, in the scratch the caller provides (P*H halves)
+    cudaError_t e = launch_pdl(sorted_rows_kernel, num_sms * 8, 256, 0, stream, reinterpret_cast<const uint4 *>(x),
+                               sorted_pair, k, T * k, H / 8, reinterpret_cast<uint4 *>(xperm));
+    if (e != cudaSuccess) return e;
+    return launch_tc<kTcGateUp>(a, q, xperm, (long long)T * k, num_sms, smem_limit, stream);
 }
 
 cudaError_t launch_combine(const float *y, const float *topk_w, int T, int k, int H, __half *out,
@@ -584,7 +645,7 @@ cudaError_t launch_down_tc(const __half *h, const uint32_t *q, const __half *s, 
     a.T = T; a.k = k; a.P = T * k;
     a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
     a.y_out = y; a.err = err;
-    cudaError_t e = launch_tc<kTcDown>(a, q, num_sms, smem_limit, stream);
+    cudaError_t e = launch_tc<kTcDown>(a, q, h, (long long)T * k, num_sms, smem_limit, stream);
     if (e != cudaSuccess) return e;
     return launch_combine(y, topk_w, T, k, H, out, stream);
 }
