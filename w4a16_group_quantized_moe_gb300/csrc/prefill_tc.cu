@@ -18,7 +18,7 @@
 //               operand layout, one copy (step 3 reads a sorted,
 //               pair-ordered copy of the x rows made by sorted_rows_kernel;
 //               step 4 the h rows, already in sorted order)
-//   warps 2-9   dequantise the codes to fp16 ((q - z) * s, per 32-wide
+//   warps 2-17  dequantise the codes to fp16 ((q - z) * s, per 32-wide
 //               group, exact q - z from the binary16 exponent trick) into the
 //               same layout; step 3 keeps the dequantiser's pair order
 //               [k0 k4 k1 k5 k2 k6 k3 k7] (x was permuted alike: the
@@ -26,7 +26,7 @@
 //               restores natural order to match h
 //   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate in
 //               tensor memory) for each K block and commits to mbarriers
-//   warps 10-13 read the accumulators (tcgen05.ld) and finish: h =
+//   warps 18-21 read the accumulators (tcgen05.ld) and finish: h =
 //               silu(gate) * up in fp16 (step 3), or the fp32 per-pair
 //               projection y (step 4, summed per token by combine_kernel)
 // The copy ring is as deep as shared memory allows (it covers the HBM
@@ -40,9 +40,9 @@
 
 namespace moe {
 
-constexpr int kTcThreads = 448;
-constexpr int kTcProducerWarp = 0, kTcMmaWarp = 1, kTcDqWarp0 = 2, kTcDqWarps = 8;
-constexpr int kTcEpiWarp0 = 10, kTcEpiWarps = 4;
+constexpr int kTcThreads = 704;
+constexpr int kTcProducerWarp = 0, kTcMmaWarp = 1, kTcDqWarp0 = 2, kTcDqWarps = 16;
+constexpr int kTcEpiWarp0 = 18, kTcEpiWarps = 4;
 constexpr int kTcM = 128;     // weight rows per tile
 constexpr int kTcKB = 64;     // K per stage: one 128-byte row of fp16
 constexpr int kTcMaxN = 128;  // activation rows per chunk
@@ -264,15 +264,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kTcProducerWarp) {
         // ---- codes and activation rows of every K block, through the copy ring
-        int j = 0;
+        int j = 0, s = 0;
+        uint32_t ph = 0;  // stage and phase of K block j in the copy ring
         for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
             const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int r0 = it.lo + it.chunk * kTcMaxN;
             for (int kb = 0; kb < nkb; ++kb, ++j) {
-                const int s = j % S;
                 // the stage is free once the MMAs of its last use are done
                 // (every lane waits; the decision is made warp-uniform)
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ctl->t_free[s], ((j / S) & 1) ^ 1, abort_flag))) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ctl->t_free[s], ph ^ 1, abort_flag))) {
                     if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -288,6 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_2d(stg, &bmap, kb * kTcKB, r0, &ctl->t_full[s]);
                 }
                 __syncwarp();
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
             }
         }
         if (lane == 0 && *abort_flag) {
@@ -298,7 +302,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == kTcMmaWarp) {
         // ---- one thread issues the MMAs
         if (lane == 0) {
-            int j = 0, n_done = 0;
+            int n_done = 0, s = 0, s2 = 0;
+            uint32_t ph = 0, ph2 = 0;  // copy ring and A ring positions
             for (int ii = blockIdx.x; ii < n_items && !*abort_flag; ii += gridDim.x, ++n_done) {
                 const TcItem it = tc_lookup(tb, A, tiles, ii);
                 const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
@@ -311,10 +316,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_after();
                 const uint32_t dacc = tmem + (uint32_t)as * (nmat * kTcMaxN);
                 bool broke = false;
-                for (int kb = 0; kb < nkb; ++kb, ++j) {
-                    const int s = j % S, s2 = j % SA;
-                    if (!mbar_wait_bounded(&ctl->a_full[s2], (j / SA) & 1, abort_flag) ||
-                        !mbar_wait_bounded(&ctl->t_full[s], (j / S) & 1, abort_flag)) {
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait_bounded(&ctl->a_full[s2], ph2, abort_flag) ||
+                        !mbar_wait_bounded(&ctl->t_full[s], ph, abort_flag)) {
                         if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                         broke = true;
                         break;
@@ -333,6 +337,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc_commit(&ctl->t_free[s]);
                     tc_commit(&ctl->a_free[s2]);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                    if (++s2 == SA) {
+                        s2 = 0;
+                        ph2 ^= 1;
+                    }
                 }
                 if (broke) break;
                 tc_commit(&ctl->acc_full[as]);
@@ -343,53 +355,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp >= kTcDqWarp0 && warp < kTcDqWarp0 + kTcDqWarps) {
         // ---- dequantise the codes into the A tile(s)
-        const int t = tid - kTcDqWarp0 * 32;  // 0..255
-        // step 3: matrix b = t / 128, row m = t % 128, all 8 words of the K
-        // block; step 4: row m = t % 128, words [4h, 4h+4) with h = t / 128
-        const int m = t & 127, half = t >> 7;
-        const int b = nmat == 2 ? half : 0;
-        const int w0 = nmat == 2 ? 0 : 4 * half;
-        int j = 0;
+        const int t = tid - kTcDqWarp0 * 32;  // 0..511
+        // each thread: one row of the tile(s) and WPT words (one group) of
+        // the K block; the threads of a row are adjacent, so a warp reads a
+        // contiguous run of codes.  Step 3: 2 threads per row of 256 (matrix
+        // b = r / 128), 4 words each; step 4: 4 threads per row of 128, 2
+        // words each.
+        constexpr int WPT = nmat == 2 ? 4 : 2, NWB = 8 / WPT;
+        const int r = t / NWB, wb = t % NWB;
+        const int b = r / kTcM, m = r % kTcM;
+        const int w0 = wb * WPT, gi = w0 / 4;  // first word, group within the K block
+        int s = 0, s2 = 0;
+        uint32_t ph = 0, ph2 = 0;  // copy ring and A ring positions
+        // this thread's 16-byte chunks in a 128-byte-swizzled tile: row base
+        // and the XOR applied to the chunk index
+        const uint32_t rbase = (uint32_t)((m >> 3) * 1024 + (m & 7) * 128), rx = (uint32_t)(m & 7);
         for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
             const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int unit = it.tile * kTcM + m;
             const bool row_ok = unit < p.rows;
             const int n = b * p.rows + unit;
-            const size_t srow = ((size_t)it.e * p.N + n) * G;
-            const size_t zrow = ((size_t)it.e * (p.N / 8) + n / 8) * G;
+            const __half *sp = p.s + ((size_t)it.e * p.N + n) * G + gi;
+            const uint32_t *zp = p.z + ((size_t)it.e * (p.N / 8) + n / 8) * G + gi;
             const uint32_t zsh = 4u * (n & 7);
-            // scales and zero words, fetched three K blocks ahead: (scale
-            // pair, zero word of the first group, zero word of the second)
-            uint32_t f0[3] = {0, 0, 0}, f1[3] = {0, 0, 0}, f2[3] = {0, 0, 0};
-            auto fetch = [&](int kb, uint32_t (&f)[3]) {
-                f[0] = f[1] = f[2] = 0;
-                if (!row_ok || kb >= nkb) return;
-                const int g0 = kb * 2 + (nmat == 2 ? 0 : half);
-                if (g0 < G) {
-                    f[0] = (uint32_t)__half_as_ushort(__ldg(p.s + srow + g0));
-                    f[1] = __ldg(p.z + zrow + g0);
-                }
-                if (nmat == 2 && g0 + 1 < G) {
-                    f[0] |= (uint32_t)__half_as_ushort(__ldg(p.s + srow + g0 + 1)) << 16;
-                    f[2] = __ldg(p.z + zrow + g0 + 1);
-                }
+            // scale and zero word of this thread's group, fetched three K
+            // blocks ahead
+            uint32_t f0[2] = {0, 0}, f1[2] = {0, 0}, f2[2] = {0, 0};
+            auto fetch = [&](int kb, uint32_t (&f)[2]) {
+                f[0] = f[1] = 0;
+                const int g = kb * 2;  // group offset of this K block
+                if (!row_ok || kb >= nkb || g + gi >= G) return;
+                f[0] = (uint32_t)__half_as_ushort(__ldg(sp + g));
+                f[1] = __ldg(zp + g);
             };
             fetch(0, f0);
             fetch(1, f1);
             fetch(2, f2);
-            for (int kb = 0; kb < nkb; ++kb, ++j) {
-                const int s = j % S, s2 = j % SA;
-                const uint32_t sc = f0[0], zc0 = f0[1], zc1 = f0[2];
+            for (int kb = 0; kb < nkb; ++kb) {
+                const uint32_t sc = f0[0], zc = f0[1];
 #pragma unroll
-                for (int i = 0; i < 3; ++i) {
+                for (int i = 0; i < 2; ++i) {
                     f0[i] = f1[i];
                     f1[i] = f2[i];
                 }
                 fetch(kb + 3, f2);
                 // the codes of this K block have landed; the A stage is free
                 // once the MMAs of its last use are done
-                const bool w_ok = mbar_wait_bounded(&ctl->t_full[s], (j / S) & 1, abort_flag) &&
-                                  mbar_wait_bounded(&ctl->a_free[s2], ((j / SA) & 1) ^ 1, abort_flag);
+                const bool w_ok = mbar_wait_bounded(&ctl->t_full[s], ph, abort_flag) &&
+                                  mbar_wait_bounded(&ctl->a_free[s2], ph2 ^ 1, abort_flag);
                 if (!__all_sync(0xffffffffu, w_ok)) {
                     if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
@@ -397,22 +410,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint8_t *codes =
                     tring + (size_t)Gm::t_bytes * s + Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2);
                 uint8_t *At = aring + (size_t)Gm::a_bytes * s2 + b * (kTcM * kTcKB * 2);
-                const ZeroPoint zp0 = make_zero_point((zc0 >> zsh) & 0xFu);
-                const ZeroPoint zp1 = make_zero_point((zc1 >> zsh) & 0xFu);
-                const __half2 s0 = __half2half2(__ushort_as_half((unsigned short)(sc & 0xFFFFu)));
-                const __half2 s1 = __half2half2(__ushort_as_half((unsigned short)(sc >> 16)));
-                uint4 cw[2];
-                cw[0] = *reinterpret_cast<const uint4 *>(codes + w0 * 4);
-                if (nmat == 2) cw[1] = *reinterpret_cast<const uint4 *>(codes + 16);
+                const ZeroPoint zpt = make_zero_point((zc >> zsh) & 0xFu);
+                const __half2 sv = __half2half2(__ushort_as_half((unsigned short)(sc & 0xFFFFu)));
+                uint32_t cw[WPT];
+                if (WPT == 4) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(codes + w0 * 4);
+                    cw[0] = v.x; cw[1] = v.y; cw[2 % WPT] = v.z; cw[3 % WPT] = v.w;
+                } else {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(codes + w0 * 4);
+                    cw[0] = v.x; cw[1] = v.y;
+                }
 #pragma unroll
-                for (int wi = 0; wi < (nmat == 2 ? 8 : 4); ++wi) {
-                    const uint4 &v = cw[wi >> 2];
-                    const uint32_t word = (wi & 3) == 0 ? v.x : ((wi & 3) == 1 ? v.y : ((wi & 3) == 2 ? v.z : v.w));
-                    // step 3: words 0-3 are group g0, 4-7 group g0+1; step 4: one group
-                    const bool second = nmat == 2 && wi >= 4;
+                for (int wi = 0; wi < WPT; ++wi) {
                     __half2 d[4];
-                    dequant_word(word, second ? zp1 : zp0, d);
-                    const __half2 sv = second ? s1 : s0;
+                    dequant_word(cw[wi], zpt, d);
                     uint32_t u[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -429,11 +440,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         o.z = __byte_perm(u[0], u[1], 0x7632);
                         o.w = __byte_perm(u[2], u[3], 0x7632);
                     }
-                    *reinterpret_cast<uint4 *>(At + sw128(m, w0 + wi)) = o;
+                    *reinterpret_cast<uint4 *>(At + rbase + ((((uint32_t)(w0 + wi)) ^ rx) << 4)) = o;
                 }
                 fence_proxy_async();  // operands written by this thread -> tensor core reads
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->a_full[s2]);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
+                if (++s2 == SA) {
+                    s2 = 0;
+                    ph2 ^= 1;
+                }
             }
         }
     } else {
@@ -472,7 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int c = 0; c < 16; ++c) {
                             if (c0 + c < nrows) {
                                 const float gv = __uint_as_float(g[c]), uv = __uint_as_float(u[c]);
-                                const float hv = gv / (1.0f + __expf(-gv)) * uv;
+                                const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                                 p.h_out[(size_t)(r0 + c0 + c) * p.rows + unit] = __float2half_rn(hv);
                             }
                         }
