@@ -68,6 +68,35 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback", None
 
 
+def tensor_peak():
+    """Dense fp16 tensor peak in TFLOP/s: the measured bf16 cuBLAS figure
+    (fp16 and bf16 run at the same tensor rate), burst (a kernel timed alone
+    in a short step)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            v = d.get("bf16_tflops")
+            if v:
+                return float(v), "measured (MEASURED_PEAKS.json bf16_tflops, burst; fp16 = bf16 tensor rate)"
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def layer_launches(T: int) -> int:
+    """Kernels the one-call layer launches for T tokens (see capi.cu /
+    prefill_tc.cu dispatch): one cooperative kernel for decode batches;
+    otherwise route+align (one launch for T <= 32), gate/up (plus the sorted
+    x gather on the tensor-core path) and down (+ combine)."""
+    if T <= 8:
+        return 1
+    ra = 1 if T <= 32 else 2
+    if T >= 64:
+        return ra + 2 + 2
+    return ra + 1 + 2
+
+
 def active_bytes(A: int, T: int, k: int, H: int, I: int):
     """Algorithmic bytes of one layer step and of the gate/up launch."""
     from w4a16_group_quantized_moe_gb300 import inputs
@@ -135,22 +164,41 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def cpu_oracle_rate(wl, seconds: float, sets: int):
-    """Tokens/s of the CPU oracle (one thread) on a bounded sample: whole
-    layers over successive router-logit sets of the workload until `seconds`
-    of CPU work have been done."""
+def oracle_step(wl, s: int, sets: int, w13, w2, n_tok: int) -> int:
+    """One oracle step on router-logit set s: the whole layer when the batch
+    is small, else the layer's output for n_tok tokens spread over the batch
+    (each token is independent, so a sample costs in proportion)."""
     import oracle
     from w4a16_group_quantized_moe_gb300 import inputs
     sh = wl.shape
+    logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + s % sets,
+                                        wl.hot_experts, wl.hot_bias)
+    if n_tok >= sh.T:
+        oracle.moe_forward(logits, x, w13, w2, sh.k)
+        return sh.T
+    for i in range(n_tok):
+        oracle.moe_token((s * n_tok + i) * 7919 % sh.T, logits, x, w13, w2, sh.k)
+    return n_tok
+
+
+def oracle_tokens_per_step(wl) -> int:
+    # whole layers for decode batches; 4 sampled tokens per step beyond that
+    return wl.shape.T if wl.shape.T <= 8 else 4
+
+
+def cpu_oracle_rate(wl, seconds: float, sets: int):
+    """Tokens/s of the CPU oracle (one thread) on a bounded sample: steps of
+    oracle_step over successive router-logit sets of the workload until
+    `seconds` of CPU work have been done."""
+    from w4a16_group_quantized_moe_gb300 import inputs
+    sh = wl.shape
     w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
+    n_tok = oracle_tokens_per_step(wl)
     tokens = 0
     t0 = time.perf_counter()
     s = 0
     while True:
-        logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + s % sets,
-                                            wl.hot_experts, wl.hot_bias)
-        oracle.moe_forward(logits, x, w13, w2, sh.k)
-        tokens += sh.T
+        tokens += oracle_step(wl, s, sets, w13, w2, n_tok)
         s += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -177,18 +225,19 @@ def run_reference(args, wl):
     w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
     times = []
     t_start = time.perf_counter()
+    n_tok = oracle_tokens_per_step(wl)
+    toks = 0
     for s in range(args.warmup + args.steps):
-        logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + s % args.sets,
-                                            wl.hot_experts, wl.hot_bias)
         t0 = time.perf_counter()
-        oracle.moe_forward(logits, x, w13, w2, sh.k)
+        n = oracle_step(wl, s, args.sets, w13, w2, n_tok)
         if s >= min(args.warmup, 1):
             times.append(time.perf_counter() - t0)
+            toks += n
         if time.perf_counter() - t_start > budget and len(times) >= 3:
             break
     steps = len(times)
     tot = sum(times)
-    value = sh.T * steps / tot
+    value = toks / tot
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": steps, "warmup": min(args.warmup, 1),
@@ -196,8 +245,9 @@ def run_reference(args, wl):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "parallelism": "cpu, 1 thread"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} whole-layer steps of {wl.name} (T={sh.T}), "
-                                   f"router logits rotated over {args.sets} sets; run capped "
+                         "sample": f"{steps} steps of {wl.name} (T={sh.T}), each "
+                                   + ("the whole layer" if n_tok >= sh.T else f"{n_tok} sampled tokens of the layer")
+                                   + f"; router logits rotated over {args.sets} sets; run capped "
                                    f"at {budget:.0f} s of CPU time (requested {args.steps})"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -380,15 +430,28 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         rate, toks, el, n = cpu_oracle_rate(wl, args.cpu_seconds, args.sets)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} whole-layer steps ({toks} tokens) of {wl.name} over "
-                         f"{el:.1f} s, single-threaded fp64 C oracle"}
+               "sample": f"{n} steps ({toks} tokens: "
+                         + ("whole layers" if oracle_tokens_per_step(wl) >= T else "sampled tokens")
+                         + f") of {wl.name} over {el:.1f} s, single-threaded fp64 C oracle"}
 
     if rank == 0:
         fused = T <= 8
-        kernel = ("decode_layer_kernel (moe_w4a16_moe_layer, one cooperative launch)" if fused
-                  else "moe_w4a16_moe_layer (route_align, gate_up, down launches)")
-        traffic = stored_traffic(wl.name) if fused else None
         med = lambda a: float(np.median(a) * 1e3)
+        if fused:
+            roof = {"kernel": "decode_layer_kernel (moe_w4a16_moe_layer, one cooperative launch)",
+                    "bound": "hbm", "achieved": layer_gbs, "peak": peak, "unit": "GB/s",
+                    "frac": layer_gbs / peak,
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                    "traffic": stored_traffic(wl.name)}
+        else:
+            # dense contraction on the tensor cores: useful FLOPs of both GEMMs
+            P = T * k
+            flops = P * (2 * H * 2 * I + 2 * I * H)
+            tf = flops / (np.median(layer_ms) / 1e3) / 1e12
+            tpk, tsrc = tensor_peak()
+            roof = {"kernel": "tc_kernel (tcgen05) x2 + gather, route, align, combine (moe_w4a16_moe_layer)",
+                    "bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
+                    "peak_source": tsrc, "flops_per_step": flops, "traffic": None}
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
@@ -407,15 +470,12 @@ def main():
                          "p90": float(np.percentile(layer_ms, 90) * 1e3)},
             "layer_us_l2_flushed_each_step": med(flushed_ms),
             "layer_us_four_step_calls": med(four_ms),
-            "roofline": {"kernel": kernel, "bound": "hbm", "achieved": layer_gbs, "peak": peak,
-                         "unit": "GB/s", "frac": layer_gbs / peak,
-                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                         "traffic": traffic},
+            "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,
                     "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
-            "gpu_launches": (1 if fused else 3) * args.steps,
+            "gpu_launches": layer_launches(T) * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line))

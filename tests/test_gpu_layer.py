@@ -73,6 +73,9 @@ DECODE_CASES = [
 OTHER_CASES = [
     inputs.Workload("mid_T9_H512_I128_E64_k6", inputs.MoEShape(9, 512, 128, 64, 6)),
     inputs.Workload("mid_T33_H512_I128_E64_k6", inputs.MoEShape(33, 512, 128, 64, 6)),
+    inputs.Workload("tc_T128_H512_I128_E64_k6", inputs.MoEShape(128, 512, 128, 64, 6)),
+    inputs.Workload("tc_T96_H256_I160_E16_k4", inputs.MoEShape(96, 256, 160, 16, 4),
+                    hot_experts=(2, 5), hot_bias=3.0),
 ]
 
 
