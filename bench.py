@@ -256,14 +256,19 @@ def run_reference(args, wl):
     print(json.dumps(line))
 
 
+# sources the one-launch decode layer kernel is compiled from
+DECODE_LAYER_SOURCES = ("common.cuh", "decode_common.cuh", "route.cuh", "decode_layer.cuh", "decode_layer.cu",
+                        "decode_layer_spec.cu", "decode_layer_gen16.cu", "decode_layer_gen4.cu",
+                        "decode_layer_gen1.cu")
+
+
 def source_digest() -> str:
-    """Digest of the CUDA sources (to tell whether stored ncu counters still
-    describe the kernels that run)."""
-    import glob
+    """Digest of the decode layer kernel's sources (to tell whether stored
+    ncu counters still describe the kernel that runs)."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "w4a16_group_quantized_moe_gb300", "csrc", "*.cu*"))):
-        h.update(open(f, "rb").read())
+    for f in DECODE_LAYER_SOURCES:
+        h.update(open(os.path.join(ROOT, "w4a16_group_quantized_moe_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
