@@ -248,15 +248,15 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
 __device__ __forceinline__ void dec_stage_rows(const __half *src, int n, int K, int G, uint8_t *xcb,
                                                int tid, int nthreads) {
     const int KB = K / 8, nx = n * KB;
-    for (int base = 0; base < nx; base += 4 * nthreads) {
-        uint4 v[4];
+    for (int base = 0; base < nx; base += 16 * nthreads) {
+        uint4 v[16];  // up to 16 loads in flight per thread: one round trip for most batches
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 16; ++c) {
             const int i = base + tid + c * nthreads;
             v[c] = i < nx ? __ldg(reinterpret_cast<const uint4 *>(src) + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 16; ++c) {
             const int i = base + tid + c * nthreads;
             if (i < nx) *reinterpret_cast<uint4 *>(xcb + dec_xoff(i / KB, i % KB, G)) = pair_interleave(v[c]);
         }

@@ -46,6 +46,11 @@ constexpr int kTcEpiWarp0 = 18, kTcEpiWarps = 4;
 constexpr int kTcM = 128;     // weight rows per tile
 constexpr int kTcKB = 64;     // K per stage: one 128-byte row of fp16
 constexpr int kTcMaxN = 128;  // activation rows per chunk
+// dequantising warps of step 4 (128 rows per tile: 8 warps, 4 words per
+// thread, measured faster than 16 warps with 2 words)
+#ifndef TC_DOWN_DQ_WARPS
+#define TC_DOWN_DQ_WARPS 8
+#endif
 constexpr int kTcMaxStages = 8;   // copy ring
 constexpr int kTcMaxAStages = 4;  // dequantised-tile ring
 constexpr int kTcMinT = 64;   // smaller batches stay on the CUDA-core stream kernels
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&ctl->t_free[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&ctl->a_full[s], kTcDqWarps);
+            mbar_init(&ctl->a_full[s], MODE == kTcGateUp ? kTcDqWarps : TC_DOWN_DQ_WARPS);
             mbar_init(&ctl->a_free[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -354,6 +359,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait_bounded(&ctl->drain, 0, nullptr);
         }
     } else if (warp >= kTcDqWarp0 && warp < kTcDqWarp0 + kTcDqWarps) {
+      constexpr int kDqActive = MODE == kTcGateUp ? kTcDqWarps : TC_DOWN_DQ_WARPS;
+      if (warp < kTcDqWarp0 + kDqActive) {
         // ---- dequantise the codes into the A tile(s)
         const int t = tid - kTcDqWarp0 * 32;  // 0..511
         // each thread: one row of the tile(s) and WPT words (one group) of
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // contiguous run of codes.  Step 3: 2 threads per row of 256 (matrix
         // b = r / 128), 4 words each; step 4: 4 threads per row of 128, 2
         // words each.
-        constexpr int WPT = nmat == 2 ? 4 : 2, NWB = 8 / WPT;
+        constexpr int WPT = nmat * kTcM * 8 / (kDqActive * 32), NWB = 8 / WPT;
         const int r = t / NWB, wb = t % NWB;
         const int b = r / kTcM, m = r % kTcM;
         const int w0 = wb * WPT, gi = w0 / 4;  // first word, group within the K block
@@ -455,6 +462,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
+      }
     } else {
         // ---- epilogue: accumulators -> h (step 3) or y (step 4)
         const int q = warp & 3;  // tensor-memory lane quadrant of this warp

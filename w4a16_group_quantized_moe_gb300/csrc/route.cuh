@@ -97,14 +97,21 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
 // rounds scans the lane's keys in ascending expert order (first maximum =
 // lowest index), takes the warp maximum and, among lanes holding it, the
 // lowest expert index; the winner's key is cleared.  Results are identical
-// to route_token's.
+// to route_token's.  E <= 1024.
 __device__ __forceinline__ void route_token_compact(const float *__restrict__ row, int E, int k, int t,
                                                     int32_t *__restrict__ topk_ids,
                                                     float *__restrict__ topk_w, int *s_ids, float *s_w,
                                                     uint32_t *s_key) {
     const int lane = threadIdx.x & 31;
-#pragma unroll 4
-    for (int e = lane; e < E; e += 32) s_key[e] = order_key(__ldg(row + e));
+    {
+        // every load first (one memory round trip), then the keys
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = lane + 32 * j < E ? __ldg(row + lane + 32 * j) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (lane + 32 * j < E) s_key[lane + 32 * j] = order_key(v[j]);
+    }
     __syncwarp();
     int my_id = 0;
     for (int s = 0; s < k; ++s) {
