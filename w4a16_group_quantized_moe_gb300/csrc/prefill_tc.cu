@@ -329,16 +329,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t abase = smem_addr(aring + (size_t)Gm::a_bytes * s2);
-                    const uint32_t bbase = smem_addr(tring + (size_t)Gm::t_bytes * s);
+                    // descriptors of the stage's tiles; a K step of 16 advances
+                    // the start address by 32 bytes, i.e. the descriptor by 2
+                    // (shared addresses are below 2^18, so the 14-bit field
+                    // never carries)
+                    const uint64_t ad0 = tc_desc_sw128(smem_addr(aring + (size_t)Gm::a_bytes * s2));
+                    const uint64_t bd0 = tc_desc_sw128(smem_addr(tring + (size_t)Gm::t_bytes * s));
 #pragma unroll
                     for (int ks = 0; ks < kTcKB / 16; ++ks) {
-                        const uint64_t bd = tc_desc_sw128(bbase + ks * 32);
 #pragma unroll
-                        for (int b = 0; b < nmat; ++b) {
-                            const uint64_t ad = tc_desc_sw128(abase + b * (kTcM * kTcKB * 2) + ks * 32);
-                            tc_mma(dacc + b * kTcMaxN, ad, bd, idesc, (kb | ks) != 0);
-                        }
+                        for (int b = 0; b < nmat; ++b)
+                            tc_mma(dacc + b * kTcMaxN, ad0 + (uint64_t)(b * (kTcM * kTcKB * 2 / 16) + ks * 2),
+                                   bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                     }
                     tc_commit(&ctl->t_free[s]);
                     tc_commit(&ctl->a_free[s2]);
