@@ -379,6 +379,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // this thread's 16-byte chunks in a 128-byte-swizzled tile: row base
         // and the XOR applied to the chunk index
         const uint32_t rbase = (uint32_t)((m >> 3) * 1024 + (m & 7) * 128), rx = (uint32_t)(m & 7);
+        // byte offsets inside a stage: this thread's codes, and its WPT
+        // chunks of the A tile ((w0 + wi) ^ rx = (w0 ^ rx) ^ wi: w0 is a
+        // multiple of WPT)
+        const uint32_t coff = Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2) + w0 * 4;
+        uint32_t aoff[WPT];
+#pragma unroll
+        for (int wi = 0; wi < WPT; ++wi)
+            aoff[wi] = (uint32_t)(b * (kTcM * kTcKB * 2)) + rbase + ((((uint32_t)w0 ^ rx) ^ (uint32_t)wi) << 4);
+        uint32_t tst = 0, ast = 0;  // byte offsets of the current copy stage and A stage
         for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
             const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int unit = it.tile * kTcM + m;
@@ -390,12 +399,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // scale and zero word of this thread's group, fetched three K
             // blocks ahead
             uint32_t f0[2] = {0, 0}, f1[2] = {0, 0}, f2[2] = {0, 0};
+            // K blocks whose group this thread has (g = 2 kb + gi < G)
+            const int kb_lim = row_ok ? min(nkb, (G - gi + 1) / 2) : 0;
             auto fetch = [&](int kb, uint32_t (&f)[2]) {
                 f[0] = f[1] = 0;
-                const int g = kb * 2;  // group offset of this K block
-                if (!row_ok || kb >= nkb || g + gi >= G) return;
-                f[0] = (uint32_t)__half_as_ushort(__ldg(sp + g));
-                f[1] = __ldg(zp + g);
+                if (kb >= kb_lim) return;
+                f[0] = (uint32_t)__half_as_ushort(__ldg(sp + 2 * kb));
+                f[1] = __ldg(zp + 2 * kb);
             };
             fetch(0, f0);
             fetch(1, f1);
@@ -410,23 +420,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 fetch(kb + 3, f2);
                 // the codes of this K block have landed; the A stage is free
                 // once the MMAs of its last use are done
-                const bool w_ok = mbar_wait_bounded(&ctl->t_full[s], ph, abort_flag) &&
-                                  mbar_wait_bounded(&ctl->a_free[s2], ph2 ^ 1, abort_flag);
+                const bool w_ok =
+                    (mbar_test(&ctl->t_full[s], ph) || mbar_wait_bounded(&ctl->t_full[s], ph, abort_flag)) &&
+                    (mbar_test(&ctl->a_free[s2], ph2 ^ 1) || mbar_wait_bounded(&ctl->a_free[s2], ph2 ^ 1, abort_flag));
                 if (!__all_sync(0xffffffffu, w_ok)) {
                     if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                const uint8_t *codes =
-                    tring + (size_t)Gm::t_bytes * s + Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2);
-                uint8_t *At = aring + (size_t)Gm::a_bytes * s2 + b * (kTcM * kTcKB * 2);
+                const uint8_t *codes = tring + tst + coff;
+                uint8_t *At = aring + ast;
                 const ZeroPoint zpt = make_zero_point((zc >> zsh) & 0xFu);
                 const __half2 sv = __half2half2(__ushort_as_half((unsigned short)(sc & 0xFFFFu)));
                 uint32_t cw[WPT];
                 if (WPT == 4) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(codes + w0 * 4);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(codes);
                     cw[0] = v.x; cw[1] = v.y; cw[2 % WPT] = v.z; cw[3 % WPT] = v.w;
                 } else {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(codes + w0 * 4);
+                    const uint2 v = *reinterpret_cast<const uint2 *>(codes);
                     cw[0] = v.x; cw[1] = v.y;
                 }
 #pragma unroll
@@ -449,17 +459,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         o.z = __byte_perm(u[0], u[1], 0x7632);
                         o.w = __byte_perm(u[2], u[3], 0x7632);
                     }
-                    *reinterpret_cast<uint4 *>(At + rbase + ((((uint32_t)(w0 + wi)) ^ rx) << 4)) = o;
+                    *reinterpret_cast<uint4 *>(At + aoff[wi]) = o;
                 }
                 fence_proxy_async();  // operands written by this thread -> tensor core reads
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->a_full[s2]);
+                tst += Gm::t_bytes;
                 if (++s == S) {
                     s = 0;
+                    tst = 0;
                     ph ^= 1;
                 }
+                ast += Gm::a_bytes;
                 if (++s2 == SA) {
                     s2 = 0;
+                    ast = 0;
                     ph2 ^= 1;
                 }
             }
