@@ -12,7 +12,7 @@
 //   3. a block-wide exclusive scan of the totals gives expert_offsets, and a
 //      scan of (total > 0) gives each active expert's slot;
 //   4. each scatter warp re-walks its slice 32 pairs at a time; lanes with the
-//      same expert find their rank among themselves with __match_any_sync, so
+//      same expert find their rank among themselves (ballots over the id bits), so
 //      the scatter keeps pair-id order inside every segment.
 #include "align.cuh"
 

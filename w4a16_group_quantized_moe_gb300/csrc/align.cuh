@@ -90,13 +90,24 @@ __device__ __forceinline__ void align_block(const int32_t *ids, int P, int E, in
 
     const int lo = warp < WS ? (int)((long long)P * warp / WS) : 0;
     const int hi = warp < WS ? (int)((long long)P * (warp + 1) / WS) : 0;
+    constexpr int kBatch = 8;  // rounds of 32 ids loaded before any is used
     bool bad = false;
-    for (int p = lo + lane; p < hi; p += 32) {
-        const int e = ids[p];
-        if (e >= 0 && e < E)
-            atomicAdd(&hist[warp * E + e], 1);
-        else
-            bad = true;
+    for (int base = lo; base < hi; base += 32 * kBatch) {
+        int ev[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int p = base + 32 * u + lane;
+            ev[u] = p < hi ? ids[p] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (base + 32 * u + lane >= hi) continue;
+            const int e = ev[u];
+            if (e >= 0 && e < E)
+                atomicAdd(&hist[warp * E + e], 1);
+            else
+                bad = true;
+        }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, MOE_DEVERR_BAD_EXPERT_ID);
     __syncthreads();
@@ -127,22 +138,41 @@ __device__ __forceinline__ void align_block(const int32_t *ids, int P, int E, in
     }
 
     // stable scatter: warps in slice order, lanes in pair order
+    const int nbits = E > 1 ? 32 - __clz(E - 1) : 0;  // bits of an expert id
     if (warp < WS) {
-        for (int base = lo; base < hi; base += 32) {
-            const int p = base + lane;
-            int e = (p < hi) ? ids[p] : -1;
-            const bool ok = (p < hi) && e >= 0 && e < E;
-            if (!ok) e = -1 - lane;  // unique key: matches only itself
-            const unsigned same = __match_any_sync(0xffffffffu, e);
-            const int rank = __popc(same & ((1u << lane) - 1u));
-            int cur = 0;
-            if (ok) {
-                cur = hist[warp * E + e];
-                sorted_pair[offs[e] + cur + rank] = p;
+        for (int b0 = lo; b0 < hi; b0 += 32 * kBatch) {
+            int ev[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int p = b0 + 32 * u + lane;
+                ev[u] = p < hi ? ids[p] : -1;
             }
-            __syncwarp();
-            if (ok && lane == 31 - __clz(same)) hist[warp * E + e] = cur + __popc(same);
-            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int base = b0 + 32 * u;
+                if (base >= hi) break;  // warp-uniform
+                const int p = base + lane;
+                int e = ev[u];
+                const bool ok = (p < hi) && e >= 0 && e < E;
+                // lanes holding the same expert: valid lanes agreeing on every
+                // bit of the id (one ballot per bit; cheaper than a match)
+                unsigned same = __ballot_sync(0xffffffffu, ok);
+                for (int bit = 0; bit < nbits; ++bit) {
+                    const bool v = (e >> bit) & 1;
+                    const unsigned bm = __ballot_sync(0xffffffffu, v);
+                    same &= v ? bm : ~bm;
+                }
+                if (!ok) same = 1u << lane;
+                const int rank = __popc(same & ((1u << lane) - 1u));
+                int cur = 0;
+                if (ok) {
+                    cur = hist[warp * E + e];
+                    sorted_pair[offs[e] + cur + rank] = p;
+                }
+                __syncwarp();
+                if (ok && lane == 31 - __clz(same)) hist[warp * E + e] = cur + __popc(same);
+                __syncwarp();
+            }
         }
     }
     // pairs with bad ids leave holes at the end; mark them

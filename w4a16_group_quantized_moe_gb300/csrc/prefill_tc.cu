@@ -12,26 +12,30 @@
 // beyond one 16-row MMA granule.
 //
 // One persistent CTA per SM, warp-specialised, all stages in shared memory:
-//   warp 0      bulk tensor copies (TMA) per 64-wide K block, into a ring
-//               of copy stages: the packed codes of the tile(s), and the
-//               chunk's activation rows in the 128-byte-swizzled K-major
-//               operand layout, one copy (step 3 reads a sorted,
-//               pair-ordered copy of the x rows made by sorted_rows_kernel;
-//               step 4 the h rows, already in sorted order)
-//   warps 2-17  dequantise the codes to fp16 ((q - z) * s, per 32-wide
+//   warp 0      bulk tensor copies (TMA) of the packed codes of the tile(s),
+//               one per 64-wide K block, into the codes ring, and an L2
+//               prefetch of the copies a few K blocks further on
+//   warp 17     bulk tensor copies of the chunk's activation rows in the
+//               128-byte-swizzled K-major operand layout into the B ring
+//               (step 3 reads a sorted, pair-ordered copy of the x rows made
+//               by sorted_rows_kernel; step 4 the h rows, already in sorted
+//               order)
+//   warps 2-..  dequantise the codes to fp16 ((q - z) * s, per 32-wide
 //               group, exact q - z from the binary16 exponent trick) into the
-//               same layout; step 3 keeps the dequantiser's pair order
-//               [k0 k4 k1 k5 k2 k6 k3 k7] (x was permuted alike: the
-//               contraction over K does not depend on the order), step 4
+//               A ring in the same layout; step 3 keeps the dequantiser's
+//               pair order [k0 k4 k1 k5 k2 k6 k3 k7] (x was permuted alike:
+//               the contraction over K does not depend on the order), step 4
 //               restores natural order to match h
 //   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate in
 //               tensor memory) for each K block and commits to mbarriers
 //   warps 18-21 read the accumulators (tcgen05.ld) and finish: h =
 //               silu(gate) * up in fp16 (step 3), or the fp32 per-pair
 //               projection y (step 4, summed per token by combine_kernel)
-// The copy ring is as deep as shared memory allows (it covers the HBM
-// latency of the codes), the dequantised tiles have their own two-stage
-// ring, and the accumulators are double-buffered, so copies,
+// Each ring is freed by its own readers: the codes ring by the dequantising
+// warps as soon as they have converted a stage, the B and A rings by the
+// MMAs that read them.  So the refill of the codes (from HBM, the longest
+// latency) never waits for the tensor core, and the small codes stages can
+// be many.  The accumulators are double-buffered, so copies,
 // dequantisation, MMA and the epilogue of consecutive tiles overlap.
 // Every wait is bounded.
 #include <cuda.h>
@@ -46,20 +50,56 @@ constexpr int kTcEpiWarp0 = 18, kTcEpiWarps = 4;
 constexpr int kTcM = 128;     // weight rows per tile
 constexpr int kTcKB = 64;     // K per stage: one 128-byte row of fp16
 constexpr int kTcMaxN = 128;  // activation rows per chunk
-// dequantising warps of step 4 (128 rows per tile: 8 warps, 4 words per
-// thread, measured faster than 16 warps with 2 words)
-#ifndef TC_DOWN_DQ_WARPS
-#define TC_DOWN_DQ_WARPS 8
+// Dequantising warps of each step.  Every thread converts WPT words of one
+// tile row per K block (a K block is 8 words of a row); fewer warps with
+// more words each spend fewer instructions on the per-stage hand-offs.
+#ifndef TC_GU_DQ_WARPS
+#define TC_GU_DQ_WARPS 8
 #endif
-constexpr int kTcMaxStages = 8;   // copy ring
-constexpr int kTcMaxAStages = 4;  // dequantised-tile ring
+#ifndef TC_DOWN_DQ_WARPS
+#define TC_DOWN_DQ_WARPS 4
+#endif
+// K blocks by which the L2 prefetch of codes and activation rows runs ahead
+// of the copies into shared memory (0: no prefetch)
+#ifndef TC_L2_AHEAD
+#define TC_L2_AHEAD 8
+#endif
+// shared-memory split: the deepest A ring (up to TC_MAX_A stages) that
+// leaves room for TC_B_STAGES activation-row stages and at least
+// TC_MIN_C_STAGES codes stages; the codes ring takes the rest
+#ifndef TC_MAX_A
+#define TC_MAX_A 3
+#endif
+#ifndef TC_B_STAGES
+#define TC_B_STAGES 4
+#endif
+#ifndef TC_MIN_C_STAGES
+#define TC_MIN_C_STAGES 4
+#endif
+constexpr int kTcMaxCStages = 16;  // codes ring
+constexpr int kTcMaxBStages = 8;   // activation-row ring
+constexpr int kTcMaxAStages = 4;   // dequantised-tile ring
+// the activation rows have their own producer: the last dequantising warp,
+// which no step uses for dequantising
+constexpr int kTcBProducerWarp = 2 + 16 - 1;
 constexpr int kTcMinT = 64;   // smaller batches stay on the CUDA-core stream kernels
 constexpr uint32_t kTcTmemCols = 512;
 
-static_assert(kTcEpiWarp0 == kTcDqWarp0 + kTcDqWarps && (kTcEpiWarp0 + kTcEpiWarps) * 32 == kTcThreads,
+static_assert(kTcEpiWarp0 == kTcDqWarp0 + kTcDqWarps && (kTcEpiWarp0 + kTcEpiWarps) * 32 == kTcThreads &&
+                  kTcBProducerWarp == kTcDqWarp0 + kTcDqWarps - 1,
               "warp roles cover the CTA");
 
 enum { kTcGateUp = 0, kTcDown = 1 };
+
+template <int MODE>
+struct TcDq {
+    static constexpr int nmat = MODE == kTcGateUp ? 2 : 1;
+    static constexpr int warps = MODE == kTcGateUp ? TC_GU_DQ_WARPS : TC_DOWN_DQ_WARPS;
+    static constexpr int wpt = nmat * kTcM * 8 / (warps * 32);  // words per thread per K block
+    static_assert(warps < kTcDqWarps && (wpt == 2 || wpt == 4 || wpt == 8) &&
+                      wpt * warps * 32 == nmat * kTcM * 8,
+                  "dequantising threads cover the tile(s): 2, 4 or 8 words each");
+};
 
 struct TcArgs {
     const __half *s;    // scales [E][N][G]
@@ -71,7 +111,7 @@ struct TcArgs {
     __half *h_out;      // step 3: [P][I]
     float *y_out;       // step 4: [P][H]
     uint32_t *err;
-    int nstages, astages;
+    int cstages, bstages, astages;  // ring depths: codes, activation rows, A tiles
     int amax;  // slot table capacity: min(E, P)
 };
 
@@ -79,18 +119,21 @@ template <int MODE>
 struct TcGeom {
     static constexpr int nmat = MODE == kTcGateUp ? 2 : 1;
     static constexpr uint32_t a_bytes = nmat * kTcM * kTcKB * 2;  // dequantised tile(s): the A ring
-    static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows   } the copy
-    static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes      } ring
-    static constexpr uint32_t t_bytes = b_bytes + c_bytes;        // multiples of 1024
+    static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows: the B ring
+    static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes: the codes ring
+    static_assert(a_bytes % 1024 == 0 && b_bytes % 1024 == 0 && c_bytes % 1024 == 0, "stage alignment");
 };
 
 // Control block after the rings: mbarriers and the tensor-memory address.
-//   t_full/t_free: copy ring (codes and activation rows of a K block)
-//   a_full/a_free: dequantised A tiles (astages stages)
+//   c_full/c_free: codes ring (freed by the dequantising warps)
+//   b_full/b_free: activation-row ring (freed by the MMAs that read it)
+//   a_full/a_free: dequantised A tiles (freed by the MMAs that read them)
 //   acc_full/acc_empty: the two accumulator buffers in tensor memory
 struct TcCtrl {
-    uint64_t t_full[kTcMaxStages];
-    uint64_t t_free[kTcMaxStages];
+    uint64_t c_full[kTcMaxCStages];
+    uint64_t c_free[kTcMaxCStages];
+    uint64_t b_full[kTcMaxBStages];
+    uint64_t b_free[kTcMaxBStages];
     uint64_t a_full[kTcMaxAStages];
     uint64_t a_free[kTcMaxAStages];
     uint64_t acc_full[2];
@@ -100,8 +143,9 @@ struct TcCtrl {
     int abort;
 };
 
-__host__ __device__ inline size_t tc_smem_bytes(uint32_t a_bytes, int astages, uint32_t t_bytes, int nstages) {
-    return 1024 + (size_t)a_bytes * astages + (size_t)t_bytes * nstages + sizeof(TcCtrl);
+__host__ __device__ inline size_t tc_smem_bytes(uint32_t a_bytes, int astages, uint32_t b_bytes, int bstages,
+                                                uint32_t c_bytes, int cstages) {
+    return 1024 + (size_t)a_bytes * astages + (size_t)b_bytes * bstages + (size_t)c_bytes * cstages + sizeof(TcCtrl);
 }
 
 // ---------------------------------------------------------------- PTX
@@ -143,6 +187,14 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// L2 prefetch of one box of a tensor map (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
     asm volatile(
@@ -199,10 +251,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int nmat = Gm::nmat;
     extern __shared__ uint8_t tc_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int S = p.nstages, SA = p.astages;
-    uint8_t *aring = smem;                             // [SA][a_bytes]
-    uint8_t *tring = smem + (size_t)SA * Gm::a_bytes;  // [S][b_bytes + c_bytes]
-    TcCtrl *ctl = reinterpret_cast<TcCtrl *>(tring + (size_t)Gm::t_bytes * S);
+    const int SC = p.cstages, SB = p.bstages, SA = p.astages;
+    uint8_t *aring = smem;                              // [SA][a_bytes]
+    uint8_t *bring = aring + (size_t)SA * Gm::a_bytes;  // [SB][b_bytes]
+    uint8_t *cring = bring + (size_t)SB * Gm::b_bytes;  // [SC][c_bytes]
+    TcCtrl *ctl = reinterpret_cast<TcCtrl *>(cring + (size_t)Gm::c_bytes * SC);
     int *tbase = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ctl) + align_up(sizeof(TcCtrl), 16));
     const TcTable tb{tbase, tbase + p.amax, tbase + 2 * p.amax, tbase + 3 * p.amax};
     int *t_tmp = tbase + 4 * p.amax + 1, *t_scratch = t_tmp + p.amax;
@@ -212,12 +265,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tiles = (p.rows + kTcM - 1) / kTcM;
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&ctl->t_full[s], 1);
-            mbar_init(&ctl->t_free[s], 1);
+        for (int s = 0; s < SC; ++s) {
+            mbar_init(&ctl->c_full[s], 1);
+            mbar_init(&ctl->c_free[s], TcDq<MODE>::warps);
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(&ctl->b_full[s], 1);
+            mbar_init(&ctl->b_free[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&ctl->a_full[s], MODE == kTcGateUp ? kTcDqWarps : TC_DOWN_DQ_WARPS);
+            mbar_init(&ctl->a_full[s], TcDq<MODE>::warps);
             mbar_init(&ctl->a_free[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -267,30 +324,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) tb.pre[A] = n_items;
     __syncthreads();
 
-    if (warp == kTcProducerWarp) {
-        // ---- codes and activation rows of every K block, through the copy ring
+    if (warp == kTcProducerWarp || warp == kTcBProducerWarp) {
+        // ---- copies of every K block: warp 0 the codes of the tile(s) (and
+        // the L2 prefetch), the B producer the chunk's activation rows; each
+        // through its own ring
+        const bool codes = warp == kTcProducerWarp;
+        const int S = codes ? SC : SB;
+        uint64_t *full = codes ? ctl->c_full : ctl->b_full;
+        uint64_t *freeb = codes ? ctl->c_free : ctl->b_free;
         int j = 0, s = 0;
-        uint32_t ph = 0;  // stage and phase of K block j in the copy ring
+        uint32_t ph = 0;  // stage and phase of K block j in the ring
+        // L2 prefetch cursor: TC_L2_AHEAD K blocks ahead in this CTA's sequence
+        int pf_ii = blockIdx.x, pf_kb = 0;
+        TcItem pf_it{};
+        if (codes && pf_ii < n_items) pf_it = tc_lookup(tb, A, tiles, pf_ii);
+        auto prefetch_next = [&]() {
+            if (pf_ii >= n_items) return;
+            if (lane == 0) {
+#pragma unroll
+                for (int b = 0; b < nmat; ++b)
+                    tma_prefetch_2d(&qmap, pf_kb * (kTcKB / 8), pf_it.e * p.N + b * p.rows + pf_it.tile * kTcM);
+                tma_prefetch_2d(&bmap, pf_kb * kTcKB, pf_it.lo + pf_it.chunk * kTcMaxN);
+            }
+            if (++pf_kb == nkb) {
+                pf_kb = 0;
+                pf_ii += gridDim.x;
+                if (pf_ii < n_items) pf_it = tc_lookup(tb, A, tiles, pf_ii);
+            }
+        };
+        if (codes)
+            for (int d = 0; d < TC_L2_AHEAD; ++d) prefetch_next();
         for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
             const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int r0 = it.lo + it.chunk * kTcMaxN;
             for (int kb = 0; kb < nkb; ++kb, ++j) {
-                // the stage is free once the MMAs of its last use are done
-                // (every lane waits; the decision is made warp-uniform)
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ctl->t_free[s], ph ^ 1, abort_flag))) {
+                if (codes && TC_L2_AHEAD > 0) prefetch_next();
+                // the stage is free once its readers are done with its last
+                // use (every lane waits; the decision is made warp-uniform)
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&freeb[s], ph ^ 1, abort_flag))) {
                     if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
                 if (lane == 0) {
-                    uint8_t *stg = tring + (size_t)Gm::t_bytes * s;
-                    mbar_arrive_expect_tx(&ctl->t_full[s], Gm::t_bytes);
+                    if (codes) {
+                        uint8_t *stg = cring + (size_t)Gm::c_bytes * s;
+                        mbar_arrive_expect_tx(&full[s], Gm::c_bytes);
 #pragma unroll
-                    for (int b = 0; b < nmat; ++b) {
-                        const int row = it.e * p.N + b * p.rows + it.tile * kTcM;
-                        tma_load_2d(stg + Gm::b_bytes + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row,
-                                    &ctl->t_full[s]);
+                        for (int b = 0; b < nmat; ++b) {
+                            const int row = it.e * p.N + b * p.rows + it.tile * kTcM;
+                            tma_load_2d(stg + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row, &full[s]);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], Gm::b_bytes);
+                        tma_load_2d(bring + (size_t)Gm::b_bytes * s, &bmap, kb * kTcKB, r0, &full[s]);
                     }
-                    tma_load_2d(stg, &bmap, kb * kTcKB, r0, &ctl->t_full[s]);
                 }
                 __syncwarp();
                 if (++s == S) {
@@ -302,13 +389,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0 && *abort_flag) {
             // never leave with a copy in flight: wait for the last issue of each stage
             for (int jj = j > S ? j - S : 0; jj < j; ++jj)
-                mbar_wait_bounded(&ctl->t_full[jj % S], (jj / S) & 1, nullptr);
+                mbar_wait_bounded(&full[jj % S], (jj / S) & 1, nullptr);
         }
     } else if (warp == kTcMmaWarp) {
         // ---- one thread issues the MMAs
         if (lane == 0) {
             int n_done = 0, s = 0, s2 = 0;
-            uint32_t ph = 0, ph2 = 0;  // copy ring and A ring positions
+            uint32_t ph = 0, ph2 = 0;  // B ring and A ring positions
             for (int ii = blockIdx.x; ii < n_items && !*abort_flag; ii += gridDim.x, ++n_done) {
                 const TcItem it = tc_lookup(tb, A, tiles, ii);
                 const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
@@ -323,7 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bool broke = false;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait_bounded(&ctl->a_full[s2], ph2, abort_flag) ||
-                        !mbar_wait_bounded(&ctl->t_full[s], ph, abort_flag)) {
+                        !mbar_wait_bounded(&ctl->b_full[s], ph, abort_flag)) {
                         if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                         broke = true;
                         break;
@@ -334,7 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // (shared addresses are below 2^18, so the 14-bit field
                     // never carries)
                     const uint64_t ad0 = tc_desc_sw128(smem_addr(aring + (size_t)Gm::a_bytes * s2));
-                    const uint64_t bd0 = tc_desc_sw128(smem_addr(tring + (size_t)Gm::t_bytes * s));
+                    const uint64_t bd0 = tc_desc_sw128(smem_addr(bring + (size_t)Gm::b_bytes * s));
 #pragma unroll
                     for (int ks = 0; ks < kTcKB / 16; ++ks) {
 #pragma unroll
@@ -342,9 +429,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             tc_mma(dacc + b * kTcMaxN, ad0 + (uint64_t)(b * (kTcM * kTcKB * 2 / 16) + ks * 2),
                                    bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                     }
-                    tc_commit(&ctl->t_free[s]);
+                    tc_commit(&ctl->b_free[s]);
                     tc_commit(&ctl->a_free[s2]);
-                    if (++s == S) {
+                    if (++s == SB) {
                         s = 0;
                         ph ^= 1;
                     }
@@ -361,33 +448,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait_bounded(&ctl->drain, 0, nullptr);
         }
     } else if (warp >= kTcDqWarp0 && warp < kTcDqWarp0 + kTcDqWarps) {
-      constexpr int kDqActive = MODE == kTcGateUp ? kTcDqWarps : TC_DOWN_DQ_WARPS;
+      constexpr int kDqActive = TcDq<MODE>::warps;
       if (warp < kTcDqWarp0 + kDqActive) {
         // ---- dequantise the codes into the A tile(s)
-        const int t = tid - kTcDqWarp0 * 32;  // 0..511
-        // each thread: one row of the tile(s) and WPT words (one group) of
-        // the K block; the threads of a row are adjacent, so a warp reads a
-        // contiguous run of codes.  Step 3: 2 threads per row of 256 (matrix
-        // b = r / 128), 4 words each; step 4: 4 threads per row of 128, 2
-        // words each.
-        constexpr int WPT = nmat * kTcM * 8 / (kDqActive * 32), NWB = 8 / WPT;
+        const int t = tid - kTcDqWarp0 * 32;
+        // each thread: one row of the tile(s) and WPT words of the K block
+        // (half a group, one group or both groups); the threads of a row are
+        // adjacent, so a warp reads a contiguous run of codes
+        constexpr int WPT = TcDq<MODE>::wpt, NWB = 8 / WPT;
+        constexpr int NG = WPT == 8 ? 2 : 1;  // groups per thread per K block
         const int r = t / NWB, wb = t % NWB;
         const int b = r / kTcM, m = r % kTcM;
-        const int w0 = wb * WPT, gi = w0 / 4;  // first word, group within the K block
+        const int w0 = wb * WPT, gi = w0 / 4;  // first word, first group within the K block
         int s = 0, s2 = 0;
-        uint32_t ph = 0, ph2 = 0;  // copy ring and A ring positions
+        uint32_t ph = 0, ph2 = 0;  // codes ring and A ring positions
         // this thread's 16-byte chunks in a 128-byte-swizzled tile: row base
         // and the XOR applied to the chunk index
         const uint32_t rbase = (uint32_t)((m >> 3) * 1024 + (m & 7) * 128), rx = (uint32_t)(m & 7);
         // byte offsets inside a stage: this thread's codes, and its WPT
         // chunks of the A tile ((w0 + wi) ^ rx = (w0 ^ rx) ^ wi: w0 is a
         // multiple of WPT)
-        const uint32_t coff = Gm::b_bytes + b * (kTcM * kTcKB / 2) + m * (kTcKB / 2) + w0 * 4;
+        const uint32_t coff = b * (kTcM * kTcKB / 2) + m * (kTcKB / 2) + w0 * 4;
         uint32_t aoff[WPT];
 #pragma unroll
         for (int wi = 0; wi < WPT; ++wi)
             aoff[wi] = (uint32_t)(b * (kTcM * kTcKB * 2)) + rbase + ((((uint32_t)w0 ^ rx) ^ (uint32_t)wi) << 4);
-        uint32_t tst = 0, ast = 0;  // byte offsets of the current copy stage and A stage
+        uint32_t tst = 0, ast = 0;  // byte offsets of the current codes stage and A stage
         for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
             const TcItem it = tc_lookup(tb, A, tiles, ii);
             const int unit = it.tile * kTcM + m;
@@ -396,24 +482,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const __half *sp = p.s + ((size_t)it.e * p.N + n) * G + gi;
             const uint32_t *zp = p.z + ((size_t)it.e * (p.N / 8) + n / 8) * G + gi;
             const uint32_t zsh = 4u * (n & 7);
-            // scale and zero word of this thread's group, fetched three K
+            // groups this thread may read: group 2 kb + gi + j of K block kb
+            const int glim = row_ok ? G - gi : 0;
+            // scale and zero word of this thread's group(s), fetched three K
             // blocks ahead
-            uint32_t f0[2] = {0, 0}, f1[2] = {0, 0}, f2[2] = {0, 0};
-            // K blocks whose group this thread has (g = 2 kb + gi < G)
-            const int kb_lim = row_ok ? min(nkb, (G - gi + 1) / 2) : 0;
-            auto fetch = [&](int kb, uint32_t (&f)[2]) {
-                f[0] = f[1] = 0;
-                if (kb >= kb_lim) return;
-                f[0] = (uint32_t)__half_as_ushort(__ldg(sp + 2 * kb));
-                f[1] = __ldg(zp + 2 * kb);
+            uint32_t f0[2 * NG], f1[2 * NG], f2[2 * NG];
+            auto fetch = [&](int kb, uint32_t (&f)[2 * NG]) {
+#pragma unroll
+                for (int j = 0; j < NG; ++j) {
+                    const bool ok = 2 * kb + j < glim;
+                    f[2 * j] = ok ? (uint32_t)__half_as_ushort(__ldg(sp + 2 * kb + j)) : 0u;
+                    f[2 * j + 1] = ok ? __ldg(zp + 2 * kb + j) : 0u;
+                }
             };
             fetch(0, f0);
             fetch(1, f1);
             fetch(2, f2);
             for (int kb = 0; kb < nkb; ++kb) {
-                const uint32_t sc = f0[0], zc = f0[1];
+                uint32_t fc[2 * NG];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < 2 * NG; ++i) {
+                    fc[i] = f0[i];
                     f0[i] = f1[i];
                     f1[i] = f2[i];
                 }
@@ -421,32 +510,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // the codes of this K block have landed; the A stage is free
                 // once the MMAs of its last use are done
                 const bool w_ok =
-                    (mbar_test(&ctl->t_full[s], ph) || mbar_wait_bounded(&ctl->t_full[s], ph, abort_flag)) &&
+                    (mbar_test(&ctl->c_full[s], ph) || mbar_wait_bounded(&ctl->c_full[s], ph, abort_flag)) &&
                     (mbar_test(&ctl->a_free[s2], ph2 ^ 1) || mbar_wait_bounded(&ctl->a_free[s2], ph2 ^ 1, abort_flag));
                 if (!__all_sync(0xffffffffu, w_ok)) {
                     if (lane == 0 && !*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                const uint8_t *codes = tring + tst + coff;
+                const uint8_t *codes = cring + tst + coff;
                 uint8_t *At = aring + ast;
-                const ZeroPoint zpt = make_zero_point((zc >> zsh) & 0xFu);
-                const __half2 sv = __half2half2(__ushort_as_half((unsigned short)(sc & 0xFFFFu)));
+                ZeroPoint zpt[NG];
+                __half2 sv[NG];
+#pragma unroll
+                for (int j = 0; j < NG; ++j) {
+                    zpt[j] = make_zero_point((fc[2 * j + 1] >> zsh) & 0xFu);
+                    sv[j] = __half2half2(__ushort_as_half((unsigned short)(fc[2 * j] & 0xFFFFu)));
+                }
                 uint32_t cw[WPT];
-                if (WPT == 4) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(codes);
-                    cw[0] = v.x; cw[1] = v.y; cw[2 % WPT] = v.z; cw[3 % WPT] = v.w;
-                } else {
+                if (WPT == 2) {
                     const uint2 v = *reinterpret_cast<const uint2 *>(codes);
-                    cw[0] = v.x; cw[1] = v.y;
+                    cw[0] = v.x; cw[1 % WPT] = v.y;
+                } else {
+#pragma unroll
+                    for (int c4 = 0; c4 < WPT / 4; ++c4) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(codes + 16 * c4);
+                        cw[(4 * c4) % WPT] = v.x; cw[(4 * c4 + 1) % WPT] = v.y;
+                        cw[(4 * c4 + 2) % WPT] = v.z; cw[(4 * c4 + 3) % WPT] = v.w;
+                    }
                 }
 #pragma unroll
                 for (int wi = 0; wi < WPT; ++wi) {
+                    const int j = wi / 4 < NG ? wi / 4 : 0;  // group of word wi
                     __half2 d[4];
-                    dequant_word(cw[wi], zpt, d);
+                    dequant_word(cw[wi], zpt[j], d);
                     uint32_t u[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const __half2 v2 = __hmul2(d[i], sv);
+                        const __half2 v2 = __hmul2(d[i], sv[j]);
                         u[i] = *reinterpret_cast<const uint32_t *>(&v2);
                     }
                     uint4 o;
@@ -463,9 +562,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 fence_proxy_async();  // operands written by this thread -> tensor core reads
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->a_full[s2]);
-                tst += Gm::t_bytes;
-                if (++s == S) {
+                if (lane == 0) {
+                    mbar_arrive(&ctl->c_free[s]);  // the warp's codes are read
+                    mbar_arrive(&ctl->a_full[s2]);
+                }
+                tst += Gm::c_bytes;
+                if (++s == SC) {
                     s = 0;
                     tst = 0;
                     ph ^= 1;
@@ -607,19 +709,24 @@ cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, const __half *brows, 
     using Gm = TcGeom<MODE>;
     TcArgs a = a0;
     a.amax = a.E < a.P ? a.E : a.P;
-    // the deepest A ring (up to 4) that leaves at least 4 copy stages
-    const size_t base = tc_smem_bytes(0, 0, 0, 0) + 16 + tc_table_bytes(a.amax);
+    // the deepest A ring (up to TC_MAX_A) that leaves room for the B ring
+    // and a codes ring of at least TC_MIN_C_STAGES; the codes ring takes the rest
+    const size_t base = tc_smem_bytes(0, 0, 0, 0, 0, 0) + 16 + tc_table_bytes(a.amax);
+    const int sb_want = TC_B_STAGES < kTcMaxBStages ? TC_B_STAGES : kTcMaxBStages;
     a.astages = 0;
-    for (int sa = kTcMaxAStages; sa >= 2; --sa)
-        if (base + (size_t)sa * Gm::a_bytes + 4 * (size_t)Gm::t_bytes <= smem_limit) {
-            a.astages = sa;
-            break;
-        }
+    for (int sa = TC_MAX_A < kTcMaxAStages ? TC_MAX_A : kTcMaxAStages; sa >= 2 && a.astages == 0; --sa)
+        for (int sb = sb_want; sb >= 2; --sb)
+            if (base + (size_t)sa * Gm::a_bytes + (size_t)sb * Gm::b_bytes + TC_MIN_C_STAGES * (size_t)Gm::c_bytes <=
+                smem_limit) {
+                a.astages = sa;
+                a.bstages = sb;
+                break;
+            }
     if (a.astages == 0) return cudaErrorInvalidConfiguration;
-    const size_t fixed = base + (size_t)a.astages * Gm::a_bytes;
-    const int S = (int)((smem_limit - fixed) / Gm::t_bytes);
-    a.nstages = S > kTcMaxStages ? kTcMaxStages : S;
-    const size_t smem = fixed + (size_t)Gm::t_bytes * a.nstages;
+    const size_t fixed = base + (size_t)a.astages * Gm::a_bytes + (size_t)a.bstages * Gm::b_bytes;
+    const int SC = (int)((smem_limit - fixed) / Gm::c_bytes);
+    a.cstages = SC > kTcMaxCStages ? kTcMaxCStages : SC;
+    const size_t smem = fixed + (size_t)Gm::c_bytes * a.cstages;
     CUtensorMap map, bmap;
     cudaError_t e = codes_map(&map, q, a.E, a.N, a.K);
     if (e != cudaSuccess) return e;
@@ -633,16 +740,33 @@ cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, const __half *brows, 
 
 // xs[r] = x[token of sorted row r], each 8-element block in the
 // dequantiser's pair order (rows of invalid pairs: zeros).  Step 3 then
-// reads the activation rows of a chunk as one contiguous tile.
+// reads the activation rows of a chunk as one contiguous tile.  One warp per
+// row: the row's pair id is read once, then up to 8 loads per lane are in
+// flight before the stores.
 __global__ void sorted_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ sorted_pair, int k,
                                    int P, int H8, uint4 *__restrict__ xs) {
     pdl_wait();
     pdl_trigger();
-    const long long n = (long long)P * H8;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const int r = (int)(i / H8), c = (int)(i - (long long)r * H8);
+    const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    const int nwarps = gridDim.x * wpb;
+    for (int r = blockIdx.x * wpb + (threadIdx.x >> 5); r < P; r += nwarps) {
         const int pr = __ldg(sorted_pair + r);
-        xs[i] = (pr >= 0 && pr < P) ? pair_interleave(__ldg(x + (size_t)(pr / k) * H8 + c)) : make_uint4(0, 0, 0, 0);
+        const bool ok = pr >= 0 && pr < P;
+        const uint4 *src = x + (size_t)(ok ? pr / k : 0) * H8;
+        uint4 *dst = xs + (size_t)r * H8;
+        for (int c0 = 0; c0 < H8; c0 += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + 32 * u + lane;
+                v[u] = (ok && c < H8) ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + 32 * u + lane;
+                if (c < H8) dst[c] = pair_interleave(v[u]);
+            }
+        }
     }
 }
 
@@ -653,7 +777,8 @@ __global__ void sorted_rows_kernel(const uint4 *__restrict__ x, const int32_t *_
 bool tc_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int amax = E < T * k ? E : T * k;
     return T >= kTcMinT && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
-           tc_smem_bytes(TcGeom<kTcGateUp>::a_bytes, 2, TcGeom<kTcGateUp>::t_bytes, 4) + 16 + tc_table_bytes(amax) <=
+           tc_smem_bytes(TcGeom<kTcGateUp>::a_bytes, 2, TcGeom<kTcGateUp>::b_bytes, 2, TcGeom<kTcGateUp>::c_bytes,
+                         TC_MIN_C_STAGES) + 16 + tc_table_bytes(amax) <=
                smem_limit;
 }
 
