@@ -4,12 +4,10 @@
 // With thousands of tokens every expert sees tens to hundreds of rows, so
 // the per-expert products of "Sparse MoE layer" (gate/up + SiLU, down) are
 // dense contractions: for expert e, D[n][r] = sum_K W_e[n][K] * act[r][K]
-// over the weight rows n of a 128-row tile and the (up to 128) activation
-// rows r of a chunk of e's segment.  The weight is the MMA's A operand
-// (M = 128 rows), the gathered activation rows its B operand (N = the chunk,
-// padded to 16): the grouping of "Active grouped decode" (active-expert
-// segments with offsets) decides the work list, and no expert is padded
-// beyond one 16-row MMA granule.
+// over the weight rows n of a 128-row tile (gate and up: both matrices'
+// tiles) and the (up to 128) activation rows r of a chunk of e's segment:
+// the grouping of "Active grouped decode" (active-expert segments with
+// offsets) decides the work list.
 //
 // One persistent CTA per SM, warp-specialised, all stages in shared memory:
 //   warp 0      bulk tensor copies (TMA) of the packed codes of the tile(s),
@@ -27,7 +25,10 @@
 //               the contraction over K does not depend on the order), step 4
 //               restores natural order to match h
 //   warp 1      one thread issues tcgen05.mma (kind::f16, fp32 accumulate in
-//               tensor memory) for each K block and commits to mbarriers
+//               tensor memory) for each K block and commits to mbarriers;
+//               step 3 puts the chunk's rows in the M = 128 slot and gate and
+//               up together in one N = 256 operand (4 MMAs per K block), step
+//               4 the weight tile in M = 128 and the chunk in N
 //   warps 18-21 read the accumulators (tcgen05.ld) and finish: h =
 //               silu(gate) * up in fp16 (step 3), or the fp32 per-pair
 //               projection y (step 4, summed per token by combine_kernel)
@@ -68,10 +69,10 @@ constexpr int kTcMaxN = 128;  // activation rows per chunk
 // leaves room for TC_B_STAGES activation-row stages and at least
 // TC_MIN_C_STAGES codes stages; the codes ring takes the rest
 #ifndef TC_MAX_A
-#define TC_MAX_A 3
+#define TC_MAX_A 4
 #endif
 #ifndef TC_B_STAGES
-#define TC_B_STAGES 4
+#define TC_B_STAGES 3
 #endif
 #ifndef TC_MIN_C_STAGES
 #define TC_MIN_C_STAGES 4
@@ -159,8 +160,8 @@ __device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
 
 // instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
 // K-major, N >> 3 at bit 17, M >> 4 at bit 24
-__device__ __forceinline__ uint32_t tc_idesc(int n) {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTcM >> 4) << 24);
+__device__ __forceinline__ uint32_t tc_idesc(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -398,15 +399,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t ph = 0, ph2 = 0;  // B ring and A ring positions
             for (int ii = blockIdx.x; ii < n_items && !*abort_flag; ii += gridDim.x, ++n_done) {
                 const TcItem it = tc_lookup(tb, A, tiles, ii);
+                // Step 3: D[chunk row][weight row] = act . W^T, the chunk's
+                // rows the A operand (M = 128; rows past the segment are
+                // ignored by the epilogue), gate and up together the B operand
+                // (N = 256): one MMA per K step.  Step 4: D[weight row][chunk
+                // row] = W . act^T (M = 128 weight rows, N = the chunk padded
+                // to 16), which lets its epilogue store fp32 rows coalesced.
                 const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
-                const uint32_t idesc = tc_idesc((nrows + 15) & ~15);
+                const uint32_t idesc = MODE == kTcGateUp ? tc_idesc(kTcMaxN, nmat * kTcM)
+                                                         : tc_idesc(kTcM, (nrows + 15) & ~15);
                 const int as = n_done & 1;
                 if (!mbar_wait_bounded(&ctl->acc_empty[as], ((n_done >> 1) & 1) ^ 1, abort_flag)) {
                     if (!*abort_flag) fail(MOE_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dacc = tmem + (uint32_t)as * (nmat * kTcMaxN);
+                const uint32_t dacc = tmem + (uint32_t)as * (nmat * kTcM);
                 bool broke = false;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait_bounded(&ctl->a_full[s2], ph2, abort_flag) ||
@@ -424,10 +432,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint64_t bd0 = tc_desc_sw128(smem_addr(bring + (size_t)Gm::b_bytes * s));
 #pragma unroll
                     for (int ks = 0; ks < kTcKB / 16; ++ks) {
-#pragma unroll
-                        for (int b = 0; b < nmat; ++b)
-                            tc_mma(dacc + b * kTcMaxN, ad0 + (uint64_t)(b * (kTcM * kTcKB * 2 / 16) + ks * 2),
-                                   bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
+                        if (MODE == kTcGateUp)
+                            tc_mma(dacc, bd0 + (uint64_t)(ks * 2), ad0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
+                        else
+                            tc_mma(dacc, ad0 + (uint64_t)(ks * 2), bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                     }
                     tc_commit(&ctl->b_free[s]);
                     tc_commit(&ctl->a_free[s2]);
@@ -595,34 +603,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (nmat * kTcMaxN);
-            const int unit = it.tile * kTcM + m;
+            const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (nmat * kTcM);
             const int r0 = it.lo + it.chunk * kTcMaxN;
-            // step 4: pair ids of the chunk's rows, lane l holding rows l + 32i
-            int prs[4] = {-1, -1, -1, -1};
-            if (MODE == kTcDown) {
+            const int u0 = it.tile * kTcM;  // first output unit of the tile
+            if (MODE == kTcGateUp) {
+                // lane m holds chunk row m (one token-expert pair), column n
+                // weight row n (gate 0..127, up 128..255): each thread
+                // finishes one pair's outputs, 16 at a time, in 32-byte
+                // stores.  Units come in runs of 16 that are wholly valid or
+                // wholly past the last row (rows is a multiple of 32), so the
+                // bound is warp-uniform.
+                const bool row_ok = m < nrows;
+                for (int c0 = 0; c0 < kTcM && u0 + c0 < p.rows; c0 += 16) {
+                    uint32_t g[16], u[16];
+                    tc_ld16(dacc + c0, g);
+                    tc_ld16(dacc + kTcM + c0, u);
+                    tc_wait_ld();
+                    if (row_ok) {
+                        uint32_t hv[8];
+#pragma unroll
+                        for (int c = 0; c < 16; c += 2) {
+                            float o[2];
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const float gv = __uint_as_float(g[c + i]), uv = __uint_as_float(u[c + i]);
+                                o[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                            }
+                            const __half2 h2 = __floats2half2_rn(o[0], o[1]);
+                            hv[c / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.h_out + (size_t)(r0 + m) * p.rows + u0 + c0);
+                        dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                        dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                    }
+                }
+            } else {
+                // lane m holds weight row m of the tile, column c chunk row
+                // c: for each column the warp stores 32 consecutive fp32
+                // outputs of one pair (pair ids: lane l holds rows l + 32i)
+                const int unit = u0 + m;
+                int prs[4] = {-1, -1, -1, -1};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (lane + 32 * i < nrows) prs[i] = __ldg(p.sorted_pair + r0 + lane + 32 * i);
-            }
-            for (int c0 = 0; c0 < nrows; c0 += 16) {
-                uint32_t g[16];
-                tc_ld16(dacc + c0, g);
-                if (MODE == kTcGateUp) {
-                    uint32_t u[16];
-                    tc_ld16(dacc + kTcMaxN + c0, u);
-                    tc_wait_ld();
-                    if (unit < p.rows) {
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            if (c0 + c < nrows) {
-                                const float gv = __uint_as_float(g[c]), uv = __uint_as_float(u[c]);
-                                const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-                                p.h_out[(size_t)(r0 + c0 + c) * p.rows + unit] = __float2half_rn(hv);
-                            }
-                        }
-                    }
-                } else {
+                for (int c0 = 0; c0 < nrows; c0 += 16) {
+                    uint32_t g[16];
+                    tc_ld16(dacc + c0, g);
                     tc_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
