@@ -4,10 +4,10 @@
 // With thousands of tokens every expert sees tens to hundreds of rows, so
 // the per-expert products of "Sparse MoE layer" (gate/up + SiLU, down) are
 // dense contractions: for expert e, D[n][r] = sum_K W_e[n][K] * act[r][K]
-// over the weight rows n of a 128-row tile (gate and up: both matrices'
-// tiles) and the (up to 128) activation rows r of a chunk of e's segment:
-// the grouping of "Active grouped decode" (active-expert segments with
-// offsets) decides the work list.
+// over the weight rows n of two 128-row tiles (the gate and up tiles of the
+// same units, or two consecutive down tiles) and the (up to 128) activation
+// rows r of a chunk of e's segment: the grouping of "Active grouped decode"
+// (active-expert segments with offsets) decides the work list.
 //
 // One persistent CTA per SM, warp-specialised, all stages in shared memory:
 //   warp 0      bulk tensor copies (TMA) of the packed codes of the tile(s),
@@ -28,7 +28,8 @@
 //               tensor memory) for each K block and commits to mbarriers;
 //               step 3 puts the chunk's rows in the M = 128 slot and gate and
 //               up together in one N = 256 operand (4 MMAs per K block), step
-//               4 the weight tile in M = 128 and the chunk in N
+//               4 each of its two weight tiles in M = 128 and the chunk in N
+//               (8 MMAs per K block)
 //   warps 18-21 read the accumulators (tcgen05.ld) and finish: h =
 //               silu(gate) * up in fp16 (step 3), or the fp32 per-pair
 //               projection y (step 4, summed per token by combine_kernel)
@@ -58,7 +59,7 @@ constexpr int kTcMaxN = 128;  // activation rows per chunk
 #define TC_GU_DQ_WARPS 8
 #endif
 #ifndef TC_DOWN_DQ_WARPS
-#define TC_DOWN_DQ_WARPS 4
+#define TC_DOWN_DQ_WARPS 8
 #endif
 // K blocks by which the L2 prefetch of codes and activation rows runs ahead
 // of the copies into shared memory (0: no prefetch)
@@ -92,9 +93,15 @@ static_assert(kTcEpiWarp0 == kTcDqWarp0 + kTcDqWarps && (kTcEpiWarp0 + kTcEpiWar
 
 enum { kTcGateUp = 0, kTcDown = 1 };
 
+// Each work item and each K-block stage covers two 128-row weight tiles:
+// the gate and up tiles of the same output units (step 3), or two
+// consecutive tiles of the down matrix (step 4).  Tile b of item tile index
+// t starts at matrix row b * tc_mat_stride + t * tc_tile_stride.
+constexpr int kTcTiles = 2;
+
 template <int MODE>
 struct TcDq {
-    static constexpr int nmat = MODE == kTcGateUp ? 2 : 1;
+    static constexpr int nmat = kTcTiles;
     static constexpr int warps = MODE == kTcGateUp ? TC_GU_DQ_WARPS : TC_DOWN_DQ_WARPS;
     static constexpr int wpt = nmat * kTcM * 8 / (warps * 32);  // words per thread per K block
     static_assert(warps < kTcDqWarps && (wpt == 2 || wpt == 4 || wpt == 8) &&
@@ -118,7 +125,7 @@ struct TcArgs {
 
 template <int MODE>
 struct TcGeom {
-    static constexpr int nmat = MODE == kTcGateUp ? 2 : 1;
+    static constexpr int nmat = kTcTiles;
     static constexpr uint32_t a_bytes = nmat * kTcM * kTcKB * 2;  // dequantised tile(s): the A ring
     static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows: the B ring
     static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes: the codes ring
@@ -244,6 +251,18 @@ __device__ __forceinline__ TcItem tc_lookup(const TcTable &tb, int A, int tiles,
 
 __host__ __device__ inline size_t tc_table_bytes(int amax) { return ((size_t)5 * amax + 1 + 128) * 4; }
 
+// Row strides of the two tiles of an item: step 3's tile b is matrix b (gate,
+// up) at the item's output units; step 4's tiles are consecutive.
+template <int MODE>
+__device__ __forceinline__ int tc_mat_stride(int rows) { return MODE == kTcGateUp ? rows : kTcM; }
+template <int MODE>
+__device__ __forceinline__ int tc_tile_stride() { return MODE == kTcGateUp ? kTcM : kTcTiles * kTcM; }
+// output unit of row m of tile b of item tile index t
+template <int MODE>
+__device__ __forceinline__ int tc_unit(int b, int t, int m) {
+    return MODE == kTcGateUp ? t * kTcM + m : (kTcTiles * t + b) * kTcM + m;
+}
+
 // ---------------------------------------------------------------- kernel
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -263,7 +282,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = p.K / 32;
     const int nkb = (p.K + kTcKB - 1) / kTcKB;
-    const int tiles = (p.rows + kTcM - 1) / kTcM;
+    // item tile indices per chunk: units per item 128 (step 3) or 256 (step 4)
+    const int tiles = (p.rows + tc_tile_stride<MODE>() - 1) / tc_tile_stride<MODE>();
+    const int mstride = tc_mat_stride<MODE>(p.rows);
 
     if (tid == 0) {
         for (int s = 0; s < SC; ++s) {
@@ -344,7 +365,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) {
 #pragma unroll
                 for (int b = 0; b < nmat; ++b)
-                    tma_prefetch_2d(&qmap, pf_kb * (kTcKB / 8), pf_it.e * p.N + b * p.rows + pf_it.tile * kTcM);
+                    tma_prefetch_2d(&qmap, pf_kb * (kTcKB / 8),
+                                    pf_it.e * p.N + b * mstride + pf_it.tile * tc_tile_stride<MODE>());
                 tma_prefetch_2d(&bmap, pf_kb * kTcKB, pf_it.lo + pf_it.chunk * kTcMaxN);
             }
             if (++pf_kb == nkb) {
@@ -372,7 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mbar_arrive_expect_tx(&full[s], Gm::c_bytes);
 #pragma unroll
                         for (int b = 0; b < nmat; ++b) {
-                            const int row = it.e * p.N + b * p.rows + it.tile * kTcM;
+                            const int row = it.e * p.N + b * mstride + it.tile * tc_tile_stride<MODE>();
                             tma_load_2d(stg + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row, &full[s]);
                         }
                     } else {
@@ -435,7 +457,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (MODE == kTcGateUp)
                             tc_mma(dacc, bd0 + (uint64_t)(ks * 2), ad0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                         else
-                            tc_mma(dacc, ad0 + (uint64_t)(ks * 2), bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
+#pragma unroll
+                            for (int b = 0; b < nmat; ++b)
+                                tc_mma(dacc + b * kTcMaxN, ad0 + (uint64_t)(b * (kTcM * kTcKB * 2 / 16) + ks * 2),
+                                       bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                     }
                     tc_commit(&ctl->b_free[s]);
                     tc_commit(&ctl->a_free[s2]);
@@ -484,9 +509,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t tst = 0, ast = 0;  // byte offsets of the current codes stage and A stage
         for (int ii = blockIdx.x; ii < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); ii += gridDim.x) {
             const TcItem it = tc_lookup(tb, A, tiles, ii);
-            const int unit = it.tile * kTcM + m;
+            const int unit = tc_unit<MODE>(b, it.tile, m);
             const bool row_ok = unit < p.rows;
-            const int n = b * p.rows + unit;
+            const int n = b * mstride + it.tile * tc_tile_stride<MODE>() + m;  // row of the expert's matrix
             const __half *sp = p.s + ((size_t)it.e * p.N + n) * G + gi;
             const uint32_t *zp = p.z + ((size_t)it.e * (p.N / 8) + n / 8) * G + gi;
             const uint32_t zsh = 4u * (n & 7);
@@ -638,17 +663,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             } else {
-                // lane m holds weight row m of the tile, column c chunk row
-                // c: for each column the warp stores 32 consecutive fp32
-                // outputs of one pair (pair ids: lane l holds rows l + 32i)
-                const int unit = u0 + m;
+                // lane m holds weight row m of tile b, column c chunk row c:
+                // for each column the warp stores 32 consecutive fp32 outputs
+                // of one pair (pair ids: lane l holds rows l + 32i)
                 int prs[4] = {-1, -1, -1, -1};
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (lane + 32 * i < nrows) prs[i] = __ldg(p.sorted_pair + r0 + lane + 32 * i);
+                for (int b = 0; b < nmat; ++b)
                 for (int c0 = 0; c0 < nrows; c0 += 16) {
+                    const int unit = tc_unit<MODE>(b, it.tile, m);
                     uint32_t g[16];
-                    tc_ld16(dacc + c0, g);
+                    tc_ld16(dacc + b * kTcMaxN + c0, g);
                     tc_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
