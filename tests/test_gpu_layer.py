@@ -76,6 +76,11 @@ OTHER_CASES = [
     inputs.Workload("tc_T128_H512_I128_E64_k6", inputs.MoEShape(128, 512, 128, 64, 6)),
     inputs.Workload("tc_T96_H256_I160_E16_k4", inputs.MoEShape(96, 256, 160, 16, 4),
                     hot_experts=(2, 5), hot_bias=3.0),
+    # tensor-core edge cases: K blocks cut short (K = 96 is 1.5 blocks of 64)
+    # and tiles past the last row; H = 384 leaves the second tile of the
+    # last down item wholly past H
+    inputs.Workload("tc_T80_H96_I96_E8_k3", inputs.MoEShape(80, 96, 96, 8, 3)),
+    inputs.Workload("tc_T64_H384_I64_E16_k2", inputs.MoEShape(64, 384, 64, 16, 2)),
 ]
 
 
