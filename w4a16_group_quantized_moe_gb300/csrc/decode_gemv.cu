@@ -1,4 +1,5 @@
-// decode_gemv.cu -- steps 3 and 4 for decode batches (T <= 8): the
+// decode_gemv.cu -- steps 3 and 4 for decode batches (T <= 16, as far as the
+// shared-memory layout allows): the
 // latency-first weight stream.
 //
 // "Active grouped decode" ("[Perf][SM70] Narrow Qwen3.8 AWQ active grouped
@@ -39,7 +40,13 @@ namespace moe {
 
 constexpr int kDecWarps = 14;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kDecMaxT = 8;   // decode batches: T <= 8
+// decode batches: T <= kDecMaxT when the layout fits in shared memory (on
+// the Qwen4Exp geometry up to 10 tokens: at 9 tokens these kernels take
+// 136 us against 297 us for the stream kernels)
+#ifndef DEC_MAX_T
+#define DEC_MAX_T 16
+#endif
+constexpr int kDecMaxT = DEC_MAX_T;
 
 struct DecodeArgs {
     const uint32_t *q;   // packed codes  [E][N][K/8]

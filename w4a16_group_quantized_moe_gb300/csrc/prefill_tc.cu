@@ -84,7 +84,13 @@ constexpr int kTcMaxAStages = 4;   // dequantised-tile ring
 // the activation rows have their own producer: the last dequantising warp,
 // which no step uses for dequantising
 constexpr int kTcBProducerWarp = 2 + 16 - 1;
-constexpr int kTcMinT = 64;   // smaller batches stay on the CUDA-core stream kernels
+// smaller batches stay on the CUDA-core kernels; above the decode kernels'
+// range the tensor-core path is 1.9-2.3x faster than the stream kernels
+// (measured on the Qwen4Exp geometry at 16-48 tokens)
+#ifndef TC_MIN_T
+#define TC_MIN_T 9
+#endif
+constexpr int kTcMinT = TC_MIN_T;
 constexpr uint32_t kTcTmemCols = 512;
 
 static_assert(kTcEpiWarp0 == kTcDqWarp0 + kTcDqWarps && (kTcEpiWarp0 + kTcEpiWarps) * 32 == kTcThreads &&
@@ -828,7 +834,8 @@ __global__ void sorted_rows_kernel(const uint4 *__restrict__ x, const int32_t *_
 // 32 (groups) and enough rows per expert on average to fill MMA granules.
 bool tc_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int amax = E < T * k ? E : T * k;
-    return T >= kTcMinT && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
+    // P >= kTcMaxN: a chunk's activation box never reaches past the sorted rows' end
+    return T >= kTcMinT && T * k >= kTcMaxN && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
            tc_smem_bytes(TcGeom<kTcGateUp>::a_bytes, 2, TcGeom<kTcGateUp>::b_bytes, 2, TcGeom<kTcGateUp>::c_bytes,
                          TC_MIN_C_STAGES) + 16 + tc_table_bytes(amax) <=
                smem_limit;
