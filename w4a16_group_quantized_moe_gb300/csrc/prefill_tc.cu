@@ -10,7 +10,7 @@
 // (active-expert segments with offsets) decides the work list.
 //
 // One persistent CTA per SM, warp-specialised, all stages in shared memory:
-//   warp 0      bulk tensor copies (TMA) of the packed codes of the tile(s),
+//   warp 0      bulk tensor copies (TMA) of the packed codes of both tiles,
 //               one per 64-wide K block, into the codes ring, and an L2
 //               prefetch of the copies a few K blocks further on
 //   warp 17     bulk tensor copies of the chunk's activation rows in the
@@ -107,12 +107,12 @@ constexpr int kTcTiles = 2;
 
 template <int MODE>
 struct TcDq {
-    static constexpr int nmat = kTcTiles;
+    static constexpr int ntile = kTcTiles;
     static constexpr int warps = MODE == kTcGateUp ? TC_GU_DQ_WARPS : TC_DOWN_DQ_WARPS;
-    static constexpr int wpt = nmat * kTcM * 8 / (warps * 32);  // words per thread per K block
+    static constexpr int wpt = ntile * kTcM * 8 / (warps * 32);  // words per thread per K block
     static_assert(warps < kTcDqWarps && (wpt == 2 || wpt == 4 || wpt == 8) &&
-                      wpt * warps * 32 == nmat * kTcM * 8,
-                  "dequantising threads cover the tile(s): 2, 4 or 8 words each");
+                      wpt * warps * 32 == ntile * kTcM * 8,
+                  "dequantising threads cover both tiles: 2, 4 or 8 words each");
 };
 
 struct TcArgs {
@@ -131,10 +131,10 @@ struct TcArgs {
 
 template <int MODE>
 struct TcGeom {
-    static constexpr int nmat = kTcTiles;
-    static constexpr uint32_t a_bytes = nmat * kTcM * kTcKB * 2;  // dequantised tile(s): the A ring
+    static constexpr int ntile = kTcTiles;
+    static constexpr uint32_t a_bytes = ntile * kTcM * kTcKB * 2;  // the two dequantised tiles: the A ring
     static constexpr uint32_t b_bytes = kTcMaxN * kTcKB * 2;      // activation rows: the B ring
-    static constexpr uint32_t c_bytes = nmat * kTcM * kTcKB / 2;  // packed codes: the codes ring
+    static constexpr uint32_t c_bytes = ntile * kTcM * kTcKB / 2;  // packed codes: the codes ring
     static_assert(a_bytes % 1024 == 0 && b_bytes % 1024 == 0 && c_bytes % 1024 == 0, "stage alignment");
 };
 
@@ -274,7 +274,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap bmap) {
     using Gm = TcGeom<MODE>;
-    constexpr int nmat = Gm::nmat;
+    constexpr int ntile = Gm::ntile;
     extern __shared__ uint8_t tc_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
     const int SC = p.cstages, SB = p.bstages, SA = p.astages;
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
 
     if (warp == kTcProducerWarp || warp == kTcBProducerWarp) {
-        // ---- copies of every K block: warp 0 the codes of the tile(s) (and
+        // ---- copies of every K block: warp 0 the codes of both tiles (and
         // the L2 prefetch), the B producer the chunk's activation rows; each
         // through its own ring
         const bool codes = warp == kTcProducerWarp;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (pf_ii >= n_items) return;
             if (lane == 0) {
 #pragma unroll
-                for (int b = 0; b < nmat; ++b)
+                for (int b = 0; b < ntile; ++b)
                     tma_prefetch_2d(&qmap, pf_kb * (kTcKB / 8),
                                     pf_it.e * p.N + b * mstride + pf_it.tile * tc_tile_stride<MODE>());
                 tma_prefetch_2d(&bmap, pf_kb * kTcKB, pf_it.lo + pf_it.chunk * kTcMaxN);
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint8_t *stg = cring + (size_t)Gm::c_bytes * s;
                         mbar_arrive_expect_tx(&full[s], Gm::c_bytes);
 #pragma unroll
-                        for (int b = 0; b < nmat; ++b) {
+                        for (int b = 0; b < ntile; ++b) {
                             const int row = it.e * p.N + b * mstride + it.tile * tc_tile_stride<MODE>();
                             tma_load_2d(stg + b * (kTcM * kTcKB / 2), &qmap, kb * (kTcKB / 8), row, &full[s]);
                         }
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // row] = W . act^T (M = 128 weight rows, N = the chunk padded
                 // to 16), which lets its epilogue store fp32 rows coalesced.
                 const int nrows = min(kTcMaxN, it.ne - it.chunk * kTcMaxN);
-                const uint32_t idesc = MODE == kTcGateUp ? tc_idesc(kTcMaxN, nmat * kTcM)
+                const uint32_t idesc = MODE == kTcGateUp ? tc_idesc(kTcMaxN, ntile * kTcM)
                                                          : tc_idesc(kTcM, (nrows + 15) & ~15);
                 const int as = n_done & 1;
                 if (!mbar_wait_bounded(&ctl->acc_empty[as], ((n_done >> 1) & 1) ^ 1, abort_flag)) {
@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dacc = tmem + (uint32_t)as * (nmat * kTcM);
+                const uint32_t dacc = tmem + (uint32_t)as * (ntile * kTcM);
                 bool broke = false;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait_bounded(&ctl->a_full[s2], ph2, abort_flag) ||
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             tc_mma(dacc, bd0 + (uint64_t)(ks * 2), ad0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                         else
 #pragma unroll
-                            for (int b = 0; b < nmat; ++b)
+                            for (int b = 0; b < ntile; ++b)
                                 tc_mma(dacc + b * kTcMaxN, ad0 + (uint64_t)(b * (kTcM * kTcKB * 2 / 16) + ks * 2),
                                        bd0 + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
                     }
@@ -489,9 +489,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= kTcDqWarp0 && warp < kTcDqWarp0 + kTcDqWarps) {
       constexpr int kDqActive = TcDq<MODE>::warps;
       if (warp < kTcDqWarp0 + kDqActive) {
-        // ---- dequantise the codes into the A tile(s)
+        // ---- dequantise the codes into the A tiles
         const int t = tid - kTcDqWarp0 * 32;
-        // each thread: one row of the tile(s) and WPT words of the K block
+        // each thread: one row of one tile and WPT words of the K block
         // (half a group, one group or both groups); the threads of a row are
         // adjacent, so a warp reads a contiguous run of codes
         constexpr int WPT = TcDq<MODE>::wpt, NWB = 8 / WPT;
@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (nmat * kTcM);
+            const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (ntile * kTcM);
             const int r0 = it.lo + it.chunk * kTcMaxN;
             const int u0 = it.tile * kTcM;  // first output unit of the tile
             if (MODE == kTcGateUp) {
@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (lane + 32 * i < nrows) prs[i] = __ldg(p.sorted_pair + r0 + lane + 32 * i);
-                for (int b = 0; b < nmat; ++b)
+                for (int b = 0; b < ntile; ++b)
                 for (int c0 = 0; c0 < nrows; c0 += 16) {
                     const int unit = tc_unit<MODE>(b, it.tile, m);
                     uint32_t g[16];
