@@ -248,7 +248,8 @@ def run_reference(args, wl):
                          "sample": f"{steps} steps of {wl.name} (T={sh.T}), each "
                                    + ("the whole layer" if n_tok >= sh.T else f"{n_tok} sampled tokens of the layer")
                                    + f"; router logits rotated over {args.sets} sets; run capped "
-                                   f"at {budget:.0f} s of CPU time (requested {args.steps})"},
+                                   f"at {budget:.0f} s of CPU time (requested {args.steps} steps after "
+                                   f"{args.warmup} warm-up; the oracle needs one untimed step)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
