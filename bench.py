@@ -84,17 +84,24 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def layer_launches(T: int) -> int:
-    """Kernels the one-call layer launches for T tokens (see capi.cu /
-    prefill_tc.cu dispatch): one cooperative kernel for decode batches;
-    otherwise route+align (one launch for T <= 32), gate/up (plus the sorted
-    x gather on the tensor-core path) and down (+ combine)."""
+def layer_launches(T: int, k: int) -> int:
+    """Kernels the one-call layer launches for T tokens, following the
+    dispatch in capi.cu, decode_gemv.cu and prefill_tc.cu.
+    - Decode batches (T <= 8): one cooperative kernel.
+    - Otherwise route+align, in one launch for T <= 32, then gate/up and
+      down.
+    - On the tensor-core path (T >= 9 and T*k >= 128): gate/up adds the
+      sorted x gather and down adds the combine.
+    - On the decode step kernels (up to 16 tokens, when their shared-memory
+      layout fits; on the benchmarked geometry that happens only below 128
+      pairs): one launch per step.
+    - On the stream kernels: down adds the combine."""
     if T <= 8:
         return 1
     ra = 1 if T <= 32 else 2
-    if T >= 64:
+    if T * k >= 128:
         return ra + 2 + 2
-    return ra + 1 + 2
+    return ra + 1 + (1 if T <= 16 else 2)
 
 
 def active_bytes(A: int, T: int, k: int, H: int, I: int):
@@ -481,7 +488,7 @@ def main():
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,
                     "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
-            "gpu_launches": layer_launches(T) * args.steps,
+            "gpu_launches": layer_launches(T, k) * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line))
