@@ -27,6 +27,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -125,7 +126,8 @@ class Clocks:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{device_index}.csv")
+        # raw samples go to a scratch file; the summary goes into the JSON line
+        self.path = os.path.join(tempfile.gettempdir(), f"moe_bench_clocks_gpu{device_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
