@@ -222,7 +222,9 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     uint32_t *err = static_cast<uint32_t *>(workspace) + kCtrlErrorWord;
-    // dispatch by shape only: decode batches take the latency-first kernel
+    // dispatch by shape only (thresholds measured): decode batches the
+    // latency-first kernels, batches that fill a 128-row chunk the tensor
+    // cores, the stream kernels in between
     if (decode_supported(T, E, k, H, I, di.smem_optin))
         return cuda_status(launch_gate_up_decode(
             reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,

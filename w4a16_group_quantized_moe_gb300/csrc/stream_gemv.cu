@@ -1,5 +1,7 @@
-// stream_gemv.cu -- steps 3 and 4 for small and mid-size batches: the
-// weight-streaming expert projections.
+// stream_gemv.cu -- steps 3 and 4 for the batches that neither the decode
+// kernels' shared-memory layout nor one 128-row tensor-core chunk fits (on
+// the Qwen4Exp geometry 11-12 tokens): the weight-streaming expert
+// projections.
 //
 // With few tokens per expert ("2-8 input tokens", "[Perf][SM70] Narrow
 // Qwen3.8 AWQ active grouped decode", section Purpose) the layer is bound
