@@ -222,6 +222,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time: every rank passes its own, every rank gets
+    the maximum (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens_per_step: int, steps: int, max_ms: float) -> float:
+    """Tokens/s of the whole job: every rank processes tokens_per_step tokens
+    per step (independent replicas), timed by the slowest rank."""
+    return world * tokens_per_step * steps / (max_ms / 1e3)
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -407,12 +425,8 @@ def main():
     four_ms = timed(n2, 0, four_calls)
     flushed_ms = timed(n2, 0, one_call, flush_each=True)
 
-    tot_ms = float(layer_ms.sum())
-    if world > 1:
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(t.item())
-    value = world * T * args.steps / (tot_ms / 1e3)
+    tot_ms = max_over_ranks(float(layer_ms.sum()), dev)
+    value = whole_job_rate(world, T, args.steps, tot_ms)
 
     lb = np.array([active_bytes(int(a), T, k, H, I)[0] for a in A_steps])
     layer_gbs = float(lb.sum() / (layer_ms.sum() / 1e3) / 1e9)
@@ -434,12 +448,8 @@ def main():
         h_out.copy_(layers[s % NL].out, non_blocking=True)
         e2e_ev[s][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(e[0].elapsed_time(e[1]) for e in e2e_ev)
-    e2e_val = T * e2e_steps / (e2e_ms / 1e3)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_val = world * T * e2e_steps / (float(t.item()) / 1e3)
+    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dev)
+    e2e_val = whole_job_rate(world, T, e2e_steps, e2e_ms)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

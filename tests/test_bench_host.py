@@ -1,6 +1,9 @@
-"""bench.py on the host, without a GPU: the reference arm (the CPU oracle)
-prints one well-formed JSON line with the benchmark's keys, and the launch
-count follows the kernel dispatch."""
+"""bench.py on the host, without a GPU:
+- the reference arm (the CPU oracle) prints one well-formed JSON line with
+  the benchmark's keys, and ranks other than 0 print nothing;
+- the launch count follows the kernel dispatch;
+- the replicas path (world size 2, gloo) times the job by its slowest rank
+  and counts every rank's tokens."""
 import json
 import os
 import subprocess
@@ -36,3 +39,46 @@ def test_launch_count_follows_the_dispatch():
     assert bench.layer_launches(4096, 10) == 6     # route, align, gather, gate/up, down, combine
     assert bench.layer_launches(32, 10) == 5       # route+align in one launch
     assert bench.layer_launches(9, 10) == 3        # decode step kernels
+
+
+def _rank_main(rank, port, q):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=2)
+    try:
+        ms = 10.0 + 5.0 * rank  # rank 1 is the slower one
+        slowest = bench.max_over_ranks(ms)
+        q.put((rank, slowest, bench.whole_job_rate(dist.get_world_size(), 4, 10, slowest)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_report_the_slowest_rank():
+    """The N > 1 bench path on CPU (gloo, world size 2): every rank gets the
+    slowest rank's time, and the whole-job rate counts both replicas' tokens."""
+    import socket
+
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, slowest, rate in got:
+        assert slowest == 15.0
+        assert abs(rate - 2 * 4 * 10 / 0.015) < 1e-6
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "1", "--workload", "tiny_T4_H256_I64_E16_k2"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
