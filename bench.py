@@ -173,46 +173,72 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def oracle_step(wl, s: int, sets: int, w13, w2, n_tok: int) -> int:
-    """One oracle step on router-logit set s: the whole layer when the batch
-    is small, else the layer's output for n_tok tokens spread over the batch
-    (each token is independent, so a sample costs in proportion)."""
+def oracle_threads() -> int:
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_plan(wl):
+    """(tokens per oracle step, threads).
+    - Decode batches run whole layers on one thread.
+    - Larger batches run a token-partitioned sample on every host core: 4
+      tokens per core, one token per call. Tokens are independent, and the C
+      oracle keeps no state and releases the interpreter lock while it runs."""
+    if wl.shape.T <= 8:
+        return wl.shape.T, 1
+    n = oracle_threads()
+    return 4 * n, n
+
+
+def oracle_step(wl, s: int, sets: int, w13, w2, n_tok: int, pool=None):
+    """One oracle step on router-logit set s.
+    - The work is the whole layer when n_tok covers the batch.
+    - Otherwise it is the outputs of n_tok tokens spread over the batch,
+      spread over the pool's threads when a pool is given.
+    - Returns (tokens, seconds spent in the oracle). Generating the inputs is
+      not timed."""
     import oracle
     from w4a16_group_quantized_moe_gb300 import inputs
     sh = wl.shape
     logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + s % sets,
                                         wl.hot_experts, wl.hot_bias)
+    t0 = time.perf_counter()
     if n_tok >= sh.T:
         oracle.moe_forward(logits, x, w13, w2, sh.k)
-        return sh.T
-    for i in range(n_tok):
-        oracle.moe_token((s * n_tok + i) * 7919 % sh.T, logits, x, w13, w2, sh.k)
-    return n_tok
-
-
-def oracle_tokens_per_step(wl) -> int:
-    # whole layers for decode batches; 4 sampled tokens per step beyond that
-    return wl.shape.T if wl.shape.T <= 8 else 4
+        return sh.T, time.perf_counter() - t0
+    toks = [(s * n_tok + i) * 7919 % sh.T for i in range(n_tok)]
+    run = lambda t: oracle.moe_token(t, logits, x, w13, w2, sh.k)
+    if pool is None:
+        for t in toks:
+            run(t)
+    else:
+        list(pool.map(run, toks))
+    return n_tok, time.perf_counter() - t0
 
 
 def cpu_oracle_rate(wl, seconds: float, sets: int):
-    """Tokens/s of the CPU oracle (one thread) on a bounded sample: steps of
-    oracle_step over successive router-logit sets of the workload until
-    `seconds` of CPU work have been done."""
+    """Tokens/s of the CPU oracle on a bounded sample (oracle_plan's
+    threads): oracle steps over successive router-logit sets of the workload
+    until `seconds` of oracle time have been spent."""
+    import concurrent.futures as cf
+
+    import oracle
     from w4a16_group_quantized_moe_gb300 import inputs
+    oracle.build()
     sh = wl.shape
     w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
-    n_tok = oracle_tokens_per_step(wl)
-    tokens = 0
-    t0 = time.perf_counter()
-    s = 0
-    while True:
-        tokens += oracle_step(wl, s, sets, w13, w2, n_tok)
-        s += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return tokens / el, tokens, el, s
+    n_tok, threads = oracle_plan(wl)
+    tokens, el, s = 0, 0.0, 0
+    with cf.ThreadPoolExecutor(threads) as pool:
+        while el < seconds:
+            n, dt = oracle_step(wl, s, sets, w13, w2, n_tok, pool if threads > 1 else None)
+            tokens += n
+            el += dt
+            s += 1
+    return tokens / el, tokens, el, s, threads
 
 
 def dist_env():
@@ -245,6 +271,8 @@ def run_reference(args, wl):
     if rank != 0:
         return
     budget = 60.0
+    import concurrent.futures as cf
+
     import oracle
     from w4a16_group_quantized_moe_gb300 import inputs
     oracle.build()
@@ -252,16 +280,16 @@ def run_reference(args, wl):
     w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
     times = []
     t_start = time.perf_counter()
-    n_tok = oracle_tokens_per_step(wl)
+    n_tok, threads = oracle_plan(wl)
     toks = 0
-    for s in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        n = oracle_step(wl, s, args.sets, w13, w2, n_tok)
-        if s >= min(args.warmup, 1):
-            times.append(time.perf_counter() - t0)
-            toks += n
-        if time.perf_counter() - t_start > budget and len(times) >= 3:
-            break
+    with cf.ThreadPoolExecutor(threads) as pool:
+        for s in range(args.warmup + args.steps):
+            n, dt = oracle_step(wl, s, args.sets, w13, w2, n_tok, pool if threads > 1 else None)
+            if s >= min(args.warmup, 1):
+                times.append(dt)
+                toks += n
+            if time.perf_counter() - t_start > budget and len(times) >= 3:
+                break
     steps = len(times)
     tot = sum(times)
     value = toks / tot
@@ -270,10 +298,12 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": steps, "warmup": min(args.warmup, 1),
         "ms_per_step": 1e3 * tot / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "parallelism": "cpu, 1 thread"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "config": {"workload": wl.name,
+                   "parallelism": f"cpu, {threads} thread{'s' if threads > 1 else ''}"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{steps} steps of {wl.name} (T={sh.T}), each "
-                                   + ("the whole layer" if n_tok >= sh.T else f"{n_tok} sampled tokens of the layer")
+                                   + ("the whole layer" if n_tok >= sh.T
+                                      else f"{n_tok} sampled tokens of the layer, one per call on {threads} threads")
                                    + f"; router logits rotated over {args.sets} sets; run capped "
                                    f"at {budget:.0f} s of CPU time (requested {args.steps} steps after "
                                    f"{args.warmup} warm-up; the oracle needs one untimed step)"},
@@ -453,11 +483,12 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        rate, toks, el, n = cpu_oracle_rate(wl, args.cpu_seconds, args.sets)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        rate, toks, el, n, threads = cpu_oracle_rate(wl, args.cpu_seconds, args.sets)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} steps ({toks} tokens: "
-                         + ("whole layers" if oracle_tokens_per_step(wl) >= T else "sampled tokens")
-                         + f") of {wl.name} over {el:.1f} s, single-threaded fp64 C oracle"}
+                         + ("whole layers" if oracle_plan(wl)[0] >= T else "sampled tokens, one per call")
+                         + f") of {wl.name} over {el:.1f} s of oracle time, fp64 C oracle on "
+                         + f"{threads} thread{'s' if threads > 1 else ''}"}
 
     if rank == 0:
         fused = T <= 8
