@@ -82,3 +82,18 @@ def test_reference_arm_other_ranks_exit_quietly():
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_large_batches_run_the_oracle_on_every_core():
+    import concurrent.futures as cf
+
+    from w4a16_group_quantized_moe_gb300 import inputs
+    small = inputs.Workload("t_T4_H256_I64_E16_k2", inputs.MoEShape(4, 256, 64, 16, 2))
+    assert bench.oracle_plan(small) == (4, 1)  # whole layers on one thread
+    wl = inputs.Workload("t_T64_H256_I64_E16_k2", inputs.MoEShape(64, 256, 64, 16, 2))
+    n_tok, threads = bench.oracle_plan(wl)
+    assert threads == bench.oracle_threads() and n_tok == 4 * threads
+    w13, w2 = inputs.make_weights(16, 256, 64, 0)
+    with cf.ThreadPoolExecutor(threads) as pool:
+        n, dt = bench.oracle_step(wl, 0, 4, w13, w2, n_tok, pool)
+    assert n == n_tok and dt > 0
