@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--flush-mb", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the secondary per-workload figures")
     ap.add_argument("--layers", type=int, default=0,
                     help="weight copies used in turn (0: enough to exceed L2 twice; 1 for profiling)")
     return ap.parse_args()
@@ -266,11 +268,42 @@ def whole_job_rate(world: int, tokens_per_step: int, steps: int, max_ms: float) 
     return world * tokens_per_step * steps / (max_ms / 1e3)
 
 
+def copies_needed(wl) -> int:
+    """Distinct weight copies a workload's steps rotate over so that every
+    step reads its active weights from HBM: enough that the other copies'
+    active weights stream more than twice the 126 MB L2 between two uses of
+    a copy (at least 4, at most 16)."""
+    from w4a16_group_quantized_moe_gb300 import inputs
+    sh = wl.shape
+    b = inputs.bytes_per_expert(sh.H, sh.I)
+    per_step = min(sh.E, sh.T * sh.k) * (b["w13"] + b["w2"])
+    return max(4, min(16, int(np.ceil(2 * 126e6 / max(per_step, 1))) + 1))
+
+
+def bench_config(wl, world: int, sets: int) -> dict:
+    """The `config` object of the JSON line: the workload, its sizes, the
+    replication and how inputs are kept larger than L2 (identical in both
+    arms)."""
+    from w4a16_group_quantized_moe_gb300 import inputs
+    sh = wl.shape
+    NL = copies_needed(wl)
+    b = inputs.bytes_per_expert(sh.H, sh.I)
+    per_step = min(sh.E, sh.T * sh.k) * (b["w13"] + b["w2"])
+    return {"workload": wl.name, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
+            "group_size": 32, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2: {NL} distinct copies of the layer's weights "
+                  f"({NL * (b['w13'] + b['w2']) * sh.E / 1e9:.1f} GB) used in turn, so the {NL - 1} steps "
+                  f"between two uses of a copy stream >= {(NL - 1) * per_step / 1e6:.0f} MB of other "
+                  f"weights through the 126 MB L2; router logits rotate over {sets} sets"}
+
+
 def run_reference(args, wl):
+    """The CPU oracle timed on the host cores, exactly --warmup untimed and
+    --steps timed steps, each a bounded sample of the workload (the whole
+    layer for decode batches, sampled tokens for large ones)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    budget = 60.0
     import concurrent.futures as cf
 
     import oracle
@@ -279,34 +312,29 @@ def run_reference(args, wl):
     sh = wl.shape
     w13, w2 = inputs.make_weights(sh.E, sh.H, sh.I, wl.seed)
     times = []
-    t_start = time.perf_counter()
     n_tok, threads = oracle_plan(wl)
     toks = 0
     with cf.ThreadPoolExecutor(threads) as pool:
         for s in range(args.warmup + args.steps):
             n, dt = oracle_step(wl, s, args.sets, w13, w2, n_tok, pool if threads > 1 else None)
-            if s >= min(args.warmup, 1):
+            if s >= args.warmup:
                 times.append(dt)
                 toks += n
-            if time.perf_counter() - t_start > budget and len(times) >= 3:
-                break
     steps = len(times)
     tot = sum(times)
     value = toks / tot
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-        "n_gpus": args.gpus, "steps": steps, "warmup": min(args.warmup, 1),
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name,
-                   "parallelism": f"cpu, {threads} thread{'s' if threads > 1 else ''}"},
+        "config": bench_config(wl, args.gpus, args.sets),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{steps} steps of {wl.name} (T={sh.T}), each "
+                         "sample": f"{steps} timed steps after {args.warmup} untimed of {wl.name} "
+                                   f"(T={sh.T}), each "
                                    + ("the whole layer" if n_tok >= sh.T
                                       else f"{n_tok} sampled tokens of the layer, one per call on {threads} threads")
-                                   + f"; router logits rotated over {args.sets} sets; run capped "
-                                   f"at {budget:.0f} s of CPU time (requested {args.steps} steps after "
-                                   f"{args.warmup} warm-up; the oracle needs one untimed step)"},
+                                   + f"; router logits rotated over {args.sets} sets; fp64 C oracle"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -344,6 +372,129 @@ def stored_traffic(workload: str):
     return float(e["dram_bytes_per_launch"])
 
 
+class LayerRig:
+    """One workload on the GPU: NL weight copies (a stack of MoE layers, used
+    in turn), `sets` router-logit/activation sets, bound layer calls, and
+    per-step CUDA-event timing on the launching stream."""
+
+    def __init__(self, moe, wl, copies, dev, sets: int, NL: int):
+        import torch
+        from w4a16_group_quantized_moe_gb300 import inputs
+        sh = wl.shape
+        self.wl, self.sh, self.moe, self.dev = wl, sh, moe, dev
+        self.NL = min(NL, len(copies))
+        self.layers = [moe.MoELayer(c13, c2, sh.T, sh.k, device=dev) for c13, c2 in copies[:self.NL]]
+        self.sets = []
+        for si in range(sets):
+            lg, xx = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + si, wl.hot_experts, wl.hot_bias)
+            self.sets.append((torch.from_numpy(lg).to(dev), torch.from_numpy(xx).to(dev)))
+        self.logits_buf = torch.empty((sh.T, sh.E), dtype=torch.float32, device=dev)
+        self.x_buf = torch.empty((sh.T, sh.H), dtype=torch.float16, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.steps4 = [ly.bind(self.logits_buf, self.x_buf, self.stream) for ly in self.layers]
+        self.calls = [ly.layer_call for ly in self.layers]
+        # active experts of every set (for the algorithmic bytes)
+        self.A_of = []
+        r0, a0, _, _ = self.steps4[0]
+        for lg, xx in self.sets:
+            self.logits_buf.copy_(lg)
+            r0(); a0()
+            self.A_of.append(int(self.layers[0].meta[3].item()))
+
+    def stage(self, s):
+        lg, xx = self.sets[s % len(self.sets)]
+        self.logits_buf.copy_(lg, non_blocking=True)
+        self.x_buf.copy_(xx, non_blocking=True)
+
+    def one_call(self, s):
+        self.calls[s % self.NL]()
+
+    def four_calls(self, s):
+        r, a_, g, d = self.steps4[s % self.NL]
+        r(); a_(); g(); d()
+
+    def timed(self, n, first, fn, flush=None):
+        """Per-step milliseconds of fn over n steps starting at step `first`."""
+        import torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        for j in range(n):
+            s = first + j
+            self.stage(s)
+            if flush is not None:
+                flush()
+            else:
+                # keep the GPU busy (~100 us) while the host enqueues the step, so
+                # host launch gaps never fall inside the events
+                torch.cuda._sleep(200000)
+            ev[j][0].record(self.stream)
+            fn(s)
+            ev[j][1].record(self.stream)
+        torch.cuda.synchronize()
+        return np.array([e[0].elapsed_time(e[1]) for e in ev])
+
+    def check_errors(self, when):
+        for ly in self.layers:
+            flag = self.moe.moe_get_device_error(ly.workspace)
+            if flag:
+                raise RuntimeError(f"device error word 0x{flag:x} {when}")
+
+    def A_steps(self, first, n):
+        return np.array([self.A_of[(first + s) % len(self.sets)] for s in range(n)])
+
+
+def roofline_entry(wl, ms, A_steps):
+    """Roofline of one workload from per-step times: HBM bytes for decode
+    batches, tensor FLOPs otherwise (the algorithmic work)."""
+    sh = wl.shape
+    T, H, I, k = sh.T, sh.H, sh.I, sh.k
+    if T <= 8:
+        lb = np.array([active_bytes(int(a), T, k, H, I)[0] for a in A_steps])
+        gbs = float(lb.sum() / (ms.sum() / 1e3) / 1e9)
+        peak, kind, _ = peaks()
+        return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                "peak_source": f"{kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "bytes_per_step": float(lb.mean())}
+    flops = T * k * (2 * H * 2 * I + 2 * I * H)
+    tf = flops / (ms.mean() / 1e3) / 1e12
+    tpk, tsrc = tensor_peak()
+    return {"bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
+            "peak_source": tsrc, "flops_per_step": flops}
+
+
+def per_config_figures(moe, dev, geoms, names, sets: int):
+    """Median/mean layer time, tokens/s and roofline fraction of each named
+    workload through the one-call layer (a few seconds of GPU time each)."""
+    from w4a16_group_quantized_moe_gb300 import inputs
+    out = []
+    for name in names:
+        wl = inputs.ALL[name]
+        copies = geoms(wl)
+        big = wl.shape.T > 8
+        rig = LayerRig(moe, wl, copies, dev, min(sets, 8), copies_needed(wl))
+        warm, steps = (3, 30) if big else (20, 400)
+        rig.timed(warm, 0, rig.one_call)
+        rig.check_errors(f"during warm-up of {name}")
+        ms = rig.timed(steps, warm, rig.one_call)
+        rig.check_errors(f"during {name}")
+        A = rig.A_steps(warm, steps)
+        roof = roofline_entry(wl, ms, A)
+        out.append({"workload": name, "steps": steps, "warmup": warm,
+                    "layer_us_median": float(np.median(ms) * 1e3), "layer_us_mean": float(ms.mean() * 1e3),
+                    "tokens_per_s": wl.shape.T * steps / (ms.sum() / 1e3),
+                    "mean_active_experts": float(A.mean()),
+                    "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")},
+                    "gpu_launches_per_step": layer_launches(wl.shape.T, wl.shape.k)})
+        del rig
+    return out
+
+
+# grouped by weight geometry, so each geometry's weights are generated once
+PER_CONFIG = ("qwen4exp_decode_T1_H2560_I640_E512_k10", "qwen4exp_decode_T2_H2560_I640_E512_k10",
+              "qwen4exp_decode_T4_H2560_I640_E512_k10", "qwen4exp_decode_T8_H2560_I640_E512_k10",
+              "qwen4exp_prefill_T4096_H2560_I640_E512_k10", "tp4shard_decode_T2_H2560_I160_E512_k10_hot16",
+              "tp4shard_decode_T4_H2560_I160_E512_k10_hot16", "tp4shard_decode_T8_H2560_I160_E512_k10_hot16")
+
+
 def main():
     args = parse()
     from w4a16_group_quantized_moe_gb300 import inputs
@@ -366,120 +517,80 @@ def main():
 
     sh = wl.shape
     T, H, I, E, k = sh.T, sh.H, sh.I, sh.E, sh.k
-    w13, w2 = inputs.make_weights(E, H, I, wl.seed)
-    dw13, dw2 = moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev)
-    del w13, w2
-    # NL distinct copies of the layer's weights (a stack of MoE layers): step s
-    # uses copy s % NL, so between two uses of a copy the other NL-1 copies'
-    # active weights stream through L2 -- more than twice its 126 MB at every
-    # workload here -- and each step reads its weights from HBM.
-    b = inputs.bytes_per_expert(H, I)
-    per_step = min(E, T * k) * (b["w13"] + b["w2"])
-    NL = args.layers if args.layers > 0 else max(4, min(16, int(np.ceil(2 * 126e6 / max(per_step, 1))) + 1))
-    layers = [moe.MoELayer(dw13, dw2, T, k, device=dev)]
-    for _ in range(NL - 1):
-        c13 = tuple(t.clone() for t in dw13)
-        c2 = tuple(t.clone() for t in dw2)
-        layers.append(moe.MoELayer(c13, c2, T, k, device=dev))
-    sets = []
-    for si in range(args.sets):
-        lg, xx = inputs.make_activations(T, H, E, wl.seed + 1000 + si, wl.hot_experts, wl.hot_bias)
-        sets.append((torch.from_numpy(lg).to(dev), torch.from_numpy(xx).to(dev)))
-    logits_buf = torch.empty((T, E), dtype=torch.float32, device=dev)
-    x_buf = torch.empty((T, H), dtype=torch.float16, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    steps4 = [ly.bind(logits_buf, x_buf, stream) for ly in layers]
-    calls = [ly.layer_call for ly in layers]
+
+    # weight copies per geometry, made once and shared by every workload of
+    # that geometry (the copies are a stack of MoE layers used in turn)
+    geo_cache = {}
+
+    def geoms(w, need=None):
+        key = (w.shape.E, w.shape.H, w.shape.I, w.seed)
+        n = max(copies_needed(w), need or 0)
+        if key not in geo_cache:
+            geo_cache.clear()
+            w13, w2 = inputs.make_weights(*key)
+            geo_cache[key] = [(moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev))]
+            del w13, w2
+        c = geo_cache[key]
+        while len(c) < n:
+            c.append((tuple(t.clone() for t in c[0][0]), tuple(t.clone() for t in c[0][1])))
+        return c
+
+    NL = args.layers if args.layers > 0 else copies_needed(wl)
+    rig = LayerRig(moe, wl, geoms(wl, NL), dev, args.sets, NL)
     flush = torch.zeros((args.flush_mb << 20) // 4, dtype=torch.float32, device=dev)
     flush_out = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush_l2():  # a read of 1 GiB: evicts every line of L2 (data and code)
         torch.sum(flush, dim=0, out=flush_out)
 
-    # active-expert count of every logits set (for the algorithmic bytes)
-    A_of = []
-    r0, a0, _, _ = steps4[0]
-    for lg, xx in sets:
-        logits_buf.copy_(lg)
-        r0(); a0()
-        A_of.append(int(layers[0].meta[3].item()))
-
-    def stage(s):
-        lg, xx = sets[s % len(sets)]
-        logits_buf.copy_(lg, non_blocking=True)
-        x_buf.copy_(xx, non_blocking=True)
-
-    def timed(n, first, fn, flush_each=False):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        for j in range(n):
-            s = first + j
-            stage(s)
-            if flush_each:
-                flush_l2()
-            else:
-                # keep the GPU busy (~100 us) while the host enqueues the step, so
-                # host launch gaps never fall inside the events
-                torch.cuda._sleep(200000)
-            ev[j][0].record(stream)
-            fn(s)
-            ev[j][1].record(stream)
-        torch.cuda.synchronize()
-        return np.array([e[0].elapsed_time(e[1]) for e in ev])
-
-    one_call = lambda s: calls[s % NL]()
-
-    def four_calls(s):
-        r, a_, g, d = steps4[s % NL]
-        r(); a_(); g(); d()
-
-    timed(args.warmup, 0, one_call)
-    timed(min(args.warmup, 50), 0, four_calls)
-    for ly in layers:
-        if moe.moe_get_device_error(ly.workspace):
-            raise RuntimeError("device error during warm-up")
-
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     with Clocks(local) as clk:
-        layer_ms = timed(args.steps, args.warmup, one_call)
-    if world > 1:
-        torch.distributed.barrier()
-    A_steps = np.array([A_of[(args.warmup + s) % len(sets)] for s in range(args.steps)])
-    for ly in layers:
-        flag = moe.moe_get_device_error(ly.workspace)
-        if flag:
-            raise RuntimeError(f"device error word 0x{flag:x} during timed steps")
-    # secondary figures: the four step calls, and one call with L2 flushed
-    n2 = min(args.steps, 2000)
-    four_ms = timed(n2, 0, four_calls)
-    flushed_ms = timed(n2, 0, one_call, flush_each=True)
+        # the sampler runs across warm-up, the timed steps and the secondary
+        # figures, so that it sees the GPU under this load for several periods
+        rig.timed(args.warmup, 0, rig.one_call)
+        rig.timed(min(args.warmup, 50), 0, rig.four_calls)
+        rig.check_errors("during warm-up")
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        layer_ms = rig.timed(args.steps, args.warmup, rig.one_call)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        rig.check_errors("during timed steps")
+        A_steps = rig.A_steps(args.warmup, args.steps)
+        # secondary figures: the four step calls, and one call with L2 flushed
+        n2 = max(200, min(args.steps, 2000))
+        four_ms = rig.timed(n2, 0, rig.four_calls)
+        flushed_ms = rig.timed(n2, 0, rig.one_call, flush=flush_l2)
+
+        # end to end through the C ABI with host buffers: H2D of the step's
+        # inputs from pinned memory, the layer call, D2H of the output
+        h_logits = [lg.cpu().pin_memory() for lg, _ in rig.sets]
+        h_x = [xx.cpu().pin_memory() for _, xx in rig.sets]
+        h_out = torch.empty((T, H), dtype=torch.float16).pin_memory()
+        e2e_steps = max(20, min(args.steps, 2000))
+        e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
+        for s in range(e2e_steps):
+            i = s % len(rig.sets)
+            e2e_ev[s][0].record(rig.stream)
+            rig.logits_buf.copy_(h_logits[i], non_blocking=True)
+            rig.x_buf.copy_(h_x[i], non_blocking=True)
+            rig.calls[s % rig.NL]()
+            h_out.copy_(rig.layers[s % rig.NL].out, non_blocking=True)
+            e2e_ev[s][1].record(rig.stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dev)
+        e2e_val = whole_job_rate(world, T, e2e_steps, e2e_ms)
+        del rig
+
+        per_config = None
+        if rank == 0 and not args.no_per_config:
+            per_config = per_config_figures(moe, dev, geoms, [n for n in PER_CONFIG if n != wl.name],
+                                            args.sets)
+    geo_cache.clear()
 
     tot_ms = max_over_ranks(float(layer_ms.sum()), dev)
     value = whole_job_rate(world, T, args.steps, tot_ms)
-
-    lb = np.array([active_bytes(int(a), T, k, H, I)[0] for a in A_steps])
-    layer_gbs = float(lb.sum() / (layer_ms.sum() / 1e3) / 1e9)
-    peak, peak_kind, _ = peaks()
-
-    # end to end through the C ABI with host buffers: H2D of the step's
-    # inputs from pinned memory, the layer call, D2H of the output
-    h_logits = [lg.cpu().pin_memory() for lg, _ in sets]
-    h_x = [xx.cpu().pin_memory() for _, xx in sets]
-    h_out = torch.empty((T, H), dtype=torch.float16).pin_memory()
-    e2e_steps = min(args.steps, 2000)
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(e2e_steps)]
-    for s in range(e2e_steps):
-        i = s % len(sets)
-        e2e_ev[s][0].record(stream)
-        logits_buf.copy_(h_logits[i], non_blocking=True)
-        x_buf.copy_(h_x[i], non_blocking=True)
-        calls[s % NL]()
-        h_out.copy_(layers[s % NL].out, non_blocking=True)
-        e2e_ev[s][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dev)
-    e2e_val = whole_job_rate(world, T, e2e_steps, e2e_ms)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -491,42 +602,28 @@ def main():
                          + f"{threads} thread{'s' if threads > 1 else ''}"}
 
     if rank == 0:
-        fused = T <= 8
         med = lambda a: float(np.median(a) * 1e3)
-        if fused:
-            roof = {"kernel": "decode_layer_kernel (moe_w4a16_moe_layer, one cooperative launch)",
-                    "bound": "hbm", "achieved": layer_gbs, "peak": peak, "unit": "GB/s",
-                    "frac": layer_gbs / peak,
-                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                    "traffic": stored_traffic(wl.name)}
+        roof = roofline_entry(wl, layer_ms, A_steps)
+        if T <= 8:
+            roof["kernel"] = "decode_layer_kernel (moe_w4a16_moe_layer, one cooperative launch)"
+            roof["traffic"] = stored_traffic(wl.name)
         else:
-            # dense contraction on the tensor cores: useful FLOPs of both GEMMs
-            P = T * k
-            flops = P * (2 * H * 2 * I + 2 * I * H)
-            tf = flops / (np.median(layer_ms) / 1e3) / 1e12
-            tpk, tsrc = tensor_peak()
-            roof = {"kernel": "tc_kernel (tcgen05) x2 + gather, route, align, combine (moe_w4a16_moe_layer)",
-                    "bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
-                    "peak_source": tsrc, "flops_per_step": flops, "traffic": None}
+            roof["kernel"] = "tc_kernel (tcgen05) x2 + gather, route, align, combine (moe_w4a16_moe_layer)"
+            roof["traffic"] = None
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16", "data": "synthetic",
-            "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k,
-                       "group_size": 32, "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2: {NL} distinct copies of the layer's weights "
-                             f"({NL * inputs.bytes_per_expert(H, I)['w13'] * E / 1e9 + NL * inputs.bytes_per_expert(H, I)['w2'] * E / 1e9:.1f} GB) "
-                             f"used in turn, so the {NL - 1} steps between two uses of a copy "
-                             f"stream >= {(NL - 1) * per_step / 1e6:.0f} MB of other weights through "
-                             f"the 126 MB L2; router logits rotate over {args.sets} sets",
-                       "mean_active_experts": float(A_steps.mean())},
-            "layer_hbm_gbs": layer_gbs,
+            "config": bench_config(wl, world, args.sets),
+            "mean_active_experts": float(A_steps.mean()),
+            "layer_hbm_gbs": roof["achieved"] if T <= 8 else None,
             "layer_us": {"median": med(layer_ms), "p10": float(np.percentile(layer_ms, 10) * 1e3),
                          "p90": float(np.percentile(layer_ms, 90) * 1e3)},
             "layer_us_l2_flushed_each_step": med(flushed_ms),
             "layer_us_four_step_calls": med(four_ms),
             "roofline": roof,
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,

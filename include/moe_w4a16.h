@@ -94,6 +94,17 @@ size_t moe_workspace_bytes(int T, int E, int k, int H, int I);
 int moe_get_device_error(void *workspace, size_t ws_bytes, uint32_t *flag_out,
                          void *stream);
 
+/* Which kernels the step calls (moe_w4a16_gate_up_silu and
+ * moe_w4a16_down_combine) run for a shape on the current device, chosen from
+ * the shape alone (host; queries the device's SM count and shared-memory
+ * limit on first use).  Returns MOE_PATH_NONE for sizes the library rejects,
+ * for T == 0 and when no device is usable. */
+#define MOE_PATH_NONE 0
+#define MOE_PATH_DECODE 1       /* latency-first weight-streaming decode kernels */
+#define MOE_PATH_TENSOR_CORE 2  /* tcgen05 grouped contractions */
+#define MOE_PATH_STREAM 3       /* staged CUDA-core streaming kernels */
+int moe_step_kernel_path(int T, int E, int k, int H, int I);
+
 /* Step 1, router.  For each token t: softmax over logits[t][0..E), the k
  * most probable experts (ties: lower expert index first), and their
  * probabilities renormalised to sum to one -- equivalently softmax over the
@@ -229,9 +240,13 @@ int moe_w4a16_moe_layer(const float *logits, const uint16_t *x,
  *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_UNSUPPORTED before
  *     anything is launched (at k = 10, H = 2560 that allows T <= 81).  Other
  *     size errors are those of moe_w4a16_down_combine.
- *   - The first call on a device looks up the scratch array's device
- *     address (with that device current); make that first call before any
- *     stream capture.
+ *   - Every call made outside stream capture looks up the scratch array's
+ *     device address on the current device, so a device reset that reloads
+ *     the library's module is harmless; a call made during capture reuses
+ *     the address of the last call on that device, so make the first call on
+ *     a device before any stream capture (otherwise MOE_ERR_CUDA).
+ *   - Argument errors are reported before anything is enqueued: a rejected
+ *     call leaves the stream and the scratch array untouched.
  *   - Every call shares the one array and it keeps the last call's contents;
  *     each call clears the parts that must start at zero (an asynchronous
  *     memset on `stream`).  Calls that overlap on the GPU, on any stream,

@@ -4,6 +4,8 @@ the CPU oracle on the same seeded inputs.
 Bars: routing ids, offsets, sorted pairs, active list and count bit-exact;
 routing weights within 1e-6; h and out within 1e-2 * max|oracle| + 1e-3
 elementwise (the layer's stated tolerance)."""
+import os
+
 import numpy as np
 import pytest
 
@@ -152,12 +154,111 @@ def test_layer_matches_oracle(moe, wl):
     assert_close(out.float().cpu().numpy(), ref["out"], f"{wl.name} out")
 
 
-def test_prefill_4096_sampled_tokens(moe):
-    """The 4096-token workload at full size; the oracle evaluates sampled
-    tokens one by one from the layer's definition."""
+def _oracle_rows(tokens, logits, x, w13, w2, k):
+    """out rows of the given tokens from the oracle's per-token evaluation,
+    spread over the host cores (each call is independent and releases the
+    interpreter lock)."""
+    import concurrent.futures as cf
+    n = max(1, min(32, os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(n) as pool:
+        rows = list(pool.map(lambda t: oracle.moe_token(int(t), logits, x, w13, w2, k), tokens))
+    return np.stack(rows)
+
+
+def _check_h_rows(layer, tokens, ids_ref, x, w13, k, E):
+    """h rows of every pair of the given tokens against the oracle's gate/up
+    on sub-batches of those tokens (h of a pair depends on its token and
+    expert only; the sub-batches run on the host cores).  The GPU's h is in
+    sorted-row order of the full batch."""
+    import concurrent.futures as cf
+    tokens = np.asarray(tokens)
+    sp_full = layer.meta[1].cpu().numpy()
+    row_of_pair = np.empty_like(sp_full)
+    row_of_pair[sp_full] = np.arange(len(sp_full), dtype=sp_full.dtype)
+    h_gpu = layer.h.float().cpu().numpy()
+
+    def part(toks):
+        sub_meta = oracle.align(np.ascontiguousarray(ids_ref[toks]), E)
+        rh = oracle.gate_up_silu(np.ascontiguousarray(x[toks]), w13, sub_meta, k)
+        full_pairs = np.array([toks[p // k] * k + p % k for p in sub_meta[1]])
+        return h_gpu[row_of_pair[full_pairs]], rh
+
+    n = max(1, min(32, os.cpu_count() or 1))
+    parts = np.array_split(tokens, max(1, min(len(tokens), 4 * n)))
+    with cf.ThreadPoolExecutor(n) as pool:
+        res = list(pool.map(part, [p for p in parts if len(p)]))
+    assert_close(np.concatenate([g for g, _ in res]), np.concatenate([r for _, r in res]),
+                 "h rows of the sampled tokens")
+
+
+def _tokens_covering_every_chunk(sp, offs, act, na, k, per_chunk=2, chunk=128, min_rows=1):
+    """Tokens whose pairs sit at the start and end of every 128-row chunk of
+    every expert's segment of at least min_rows rows (so every tensor-core
+    work item of those experts is checked)."""
+    toks = set()
+    for e in act[:na]:
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        if hi - lo < min_rows:
+            continue
+        for c0 in range(lo, hi, chunk):
+            c1 = min(hi, c0 + chunk)
+            for r in list(range(c0, min(c1, c0 + per_chunk))) + list(range(max(c0, c1 - per_chunk), c1)):
+                toks.add(int(sp[r]) // k)
+    return sorted(toks)
+
+
+def test_prefill_4096_every_token(moe):
+    """The 4096-token workload at full size: routing and grouping bit-exact,
+    every token's output against the oracle's per-token evaluation, and the
+    h rows of the tokens at both ends of every tensor-core chunk."""
     wl = inputs.PREFILL
     sh = wl.shape
     logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed)
+    w13, w2, dw13, dw2 = weights(sh.E, sh.H, sh.I, wl.seed)
+    layer, out = run_layer(moe, logits, x, dw13, dw2, sh.k)
+    assert moe.moe_step_kernel_path(sh.T, sh.E, sh.k, sh.H, sh.I) == moe.MOE_PATH_TENSOR_CORE
+    ids_ref, w_ref = oracle.route(logits, sh.k)
+    assert np.array_equal(layer.topk_ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(layer.topk_w.cpu().numpy(), w_ref, rtol=0, atol=1e-6)
+    r_offs, r_sp, r_act, r_na = oracle.align(ids_ref, sh.E)
+    offs, sp, act, na = (t.cpu().numpy() for t in layer.meta)
+    assert np.array_equal(offs, r_offs) and np.array_equal(sp, r_sp)
+    assert np.array_equal(act, r_act) and int(na[0]) == r_na
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    ref = _oracle_rows(range(sh.T), logits, x, w13, w2, sh.k)
+    assert_close(got, ref, "prefill out, every token")
+    toks = _tokens_covering_every_chunk(r_sp, r_offs, r_act, r_na, sh.k, per_chunk=1)
+    _check_h_rows(layer, toks, ids_ref, x, w13, sh.k, sh.E)
+
+
+# Routing skewed so that hot experts' segments span several 128-row chunks of
+# the tensor-core path (chunk index >= 1): all tokens checked at the small
+# shape, and at the Qwen4Exp TP4-shard shape the tokens at both ends of every
+# chunk plus their h rows.
+def test_tensor_core_multi_chunk_segments_small(moe):
+    wl = inputs.Workload("tcskew_T512_H512_I128_E16_k4_hot2", inputs.MoEShape(512, 512, 128, 16, 4),
+                         hot_experts=(3, 9), hot_bias=6.0)
+    sh = wl.shape
+    assert moe.moe_step_kernel_path(sh.T, sh.E, sh.k, sh.H, sh.I) == moe.MOE_PATH_TENSOR_CORE
+    logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed, wl.hot_experts, wl.hot_bias)
+    w13, w2, dw13, dw2 = weights(sh.E, sh.H, sh.I, wl.seed)
+    layer, out = run_layer(moe, logits, x, dw13, dw2, sh.k)
+    ref = oracle.moe_forward(logits, x, w13, w2, sh.k)
+    offs = ref["expert_offsets"]
+    assert max(np.diff(offs)) > 3 * 128          # a segment of four chunks
+    assert np.array_equal(layer.topk_ids.cpu().numpy(), ref["topk_ids"])
+    check_meta(layer, ref, sh.E)
+    assert_close(layer.h.float().cpu().numpy(), ref["h"], f"{wl.name} h")
+    assert_close(out.float().cpu().numpy(), ref["out"], f"{wl.name} out")
+
+
+def test_tensor_core_multi_chunk_segments_tp4_shape(moe):
+    wl = inputs.Workload("tp4shard_T2048_H2560_I160_E512_k10_hot16", inputs.MoEShape(2048, 2560, 160, 512, 10),
+                         hot_experts=tuple(range(16)), hot_bias=2.0)
+    sh = wl.shape
+    assert moe.moe_step_kernel_path(sh.T, sh.E, sh.k, sh.H, sh.I) == moe.MOE_PATH_TENSOR_CORE
+    logits, x = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed, wl.hot_experts, wl.hot_bias)
     w13, w2, dw13, dw2 = weights(sh.E, sh.H, sh.I, wl.seed)
     layer, out = run_layer(moe, logits, x, dw13, dw2, sh.k)
     ids_ref, _ = oracle.route(logits, sh.k)
@@ -166,11 +267,14 @@ def test_prefill_4096_sampled_tokens(moe):
     offs, sp, act, na = (t.cpu().numpy() for t in layer.meta)
     assert np.array_equal(offs, r_offs) and np.array_equal(sp, r_sp)
     assert np.array_equal(act, r_act) and int(na[0]) == r_na
+    assert max(np.diff(r_offs)) > 4 * 128        # hot segments of five or more chunks
+    toks = _tokens_covering_every_chunk(r_sp, r_offs, r_act, r_na, sh.k, per_chunk=1)
     got = out.float().cpu().numpy()
-    sample = [0, 1, 2047, 4095] + list(np.random.default_rng(0).choice(sh.T, 8, replace=False))
-    ref_rows = np.stack([oracle.moe_token(t, logits, x, w13, w2, sh.k) for t in sample])
-    assert_close(got[sample], ref_rows, "prefill sampled out")
     assert np.all(np.isfinite(got))
+    assert_close(got[toks], _oracle_rows(toks, logits, x, w13, w2, sh.k), "tp4 T2048 out")
+    # h: every chunk of the segments longer than one chunk
+    long_toks = _tokens_covering_every_chunk(r_sp, r_offs, r_act, r_na, sh.k, per_chunk=2, min_rows=129)
+    _check_h_rows(layer, long_toks, ids_ref, x, w13, sh.k, sh.E)
 
 
 def test_decode_and_grouped_paths_agree_at_8_9_boundary(moe):

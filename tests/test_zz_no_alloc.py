@@ -4,14 +4,16 @@ Some callers cannot call cudaMalloc (an engine that fixes its device memory
 before serving, a plugin without access to the host's allocator), so the
 library offers moe_w4a16_down_combine_noalloc, which keeps its scratch in a
 fixed array inside the library instead of a caller workspace.  Here it is
-called through the C ABI and must reproduce moe_w4a16_down_combine, twice in
-a row (the shared array keeps the previous call's contents).  This file is
-collected last on purpose."""
+called through the C ABI, on every kernel path of the step, and must agree
+with the oracle and with moe_w4a16_down_combine, twice in a row (the shared
+array keeps the previous call's contents).  This file is collected last on
+purpose."""
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from w4a16_group_quantized_moe_gb300 import inputs
 
 torch = pytest.importorskip("torch")
@@ -31,36 +33,64 @@ def moe():
     return m
 
 
-# a decode batch (fused-combine kernels) and a larger one (staged kernels)
-SHAPES = [inputs.MoEShape(4, 512, 128, 64, 6), inputs.MoEShape(12, 512, 128, 64, 6)]
+# One shape per kernel path of the down/combine step, each inside the 8 MiB
+# scratch: the decode kernels (fused combine), the staged stream kernels
+# (per-pair projections in the scratch, then the combine kernel) and the
+# tensor-core kernels (the same scratch areas through the tcgen05 path).
+SHAPES = [
+    (inputs.MoEShape(4, 512, 128, 64, 6), "MOE_PATH_DECODE"),
+    (inputs.MoEShape(12, 2560, 640, 32, 10), "MOE_PATH_STREAM"),
+    (inputs.MoEShape(64, 512, 128, 16, 4), "MOE_PATH_TENSOR_CORE"),
+]
 
 
-@pytest.mark.parametrize("sh", SHAPES, ids=lambda s: f"T{s.T}")
-def test_noalloc_matches_workspace_call_twice(moe, sh):
+def _oracle_step4_inputs(logits, x, w13, sh):
+    """Routing, grouping and h from the oracle alone; h rounded to fp16 as
+    the library stores it (the inputs of step 4)."""
+    ids, tw = oracle.route(logits, sh.k)
+    meta = oracle.align(ids, sh.E)
+    h16 = oracle.gate_up_silu(x, w13, meta, sh.k).astype(np.float16)
+    return ids, tw, meta, h16
+
+
+@pytest.mark.parametrize("sh,path", SHAPES, ids=lambda v: f"T{v.T}" if hasattr(v, "T") else v)
+def test_noalloc_matches_oracle_and_workspace_call_twice(moe, sh, path):
+    assert moe.moe_step_kernel_path(sh.T, sh.E, sh.k, sh.H, sh.I) == getattr(moe, path)
+    assert moe.workspace_bytes(sh.T, sh.E, sh.k, sh.H, sh.I) <= 8 << 20
     logits, x, w13, w2 = inputs.make_workload(inputs.Workload("na", sh), seed=7)
-    dw13, dw2 = moe.to_device_weights(w13), moe.to_device_weights(w2)
-    layer = moe.MoELayer(dw13, dw2, sh.T, sh.k)
-    ref = layer.forward(torch.from_numpy(logits).cuda(), torch.from_numpy(x).cuda()).clone()
-    torch.cuda.synchronize()
-    assert moe.moe_get_device_error(layer.workspace) == 0
-    ref_np = ref.float().cpu().numpy()
-    bound = TOL_REL * np.abs(ref_np).max() + TOL_ABS
+    ids, tw, meta, h16 = _oracle_step4_inputs(logits, x, w13, sh)
+    ref_out = oracle.down_combine(h16.astype(np.float64), w2, meta, tw, sh.T, sh.k)
+    bound = TOL_REL * np.abs(ref_out).max() + TOL_ABS
+
+    dev = "cuda"
+    dw2 = moe.to_device_weights(w2)
+    d_h = torch.from_numpy(h16).to(dev)
+    d_tw = torch.from_numpy(tw.astype(np.float32)).to(dev)
+    offs, sp, act = (torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in meta[:3])
+    na = torch.tensor([meta[3]], dtype=torch.int32, device=dev)
+    d_meta = (offs, sp, act, na)
+
+    # the existing entry point with a workspace, for comparison
+    ws = moe.new_workspace(sh.T, sh.E, sh.k, sh.H, sh.I)
+    ws_out = moe.moe_w4a16_down_combine(d_h, dw2, d_meta, d_tw, ws).float().cpu().numpy()
+    assert moe.moe_get_device_error(ws) == 0
 
     lib = moe.load_library()
-    offs, sp, act, na = layer.meta
     stream = torch.cuda.current_stream().cuda_stream
     for call in range(2):
-        out = torch.full((sh.T, sh.H), float("nan"), dtype=torch.float16, device="cuda")
+        out = torch.full((sh.T, sh.H), float("nan"), dtype=torch.float16, device=dev)
         st = lib.moe_w4a16_down_combine_noalloc(
-            layer.h.data_ptr(), dw2[0].data_ptr(), dw2[1].data_ptr(), dw2[2].data_ptr(), 32,
-            offs.data_ptr(), sp.data_ptr(), act.data_ptr(), na.data_ptr(), layer.topk_w.data_ptr(),
+            d_h.data_ptr(), dw2[0].data_ptr(), dw2[1].data_ptr(), dw2[2].data_ptr(), 32,
+            offs.data_ptr(), sp.data_ptr(), act.data_ptr(), na.data_ptr(), d_tw.data_ptr(),
             sh.T, sh.E, sh.k, sh.H, sh.I, out.data_ptr(), ctypes.c_void_p(stream))
         assert st == moe.MOE_OK, f"call {call}: status {st}"
         torch.cuda.synchronize()
         got = out.float().cpu().numpy()
         assert np.all(np.isfinite(got)), f"call {call}: non-finite output"
-        err = np.abs(got - ref_np).max()
-        assert err <= bound, f"call {call}: max err {err:.3e} > {bound:.3e}"
+        err = np.abs(got - ref_out).max()
+        assert err <= bound, f"call {call}: max err vs oracle {err:.3e} > {bound:.3e}"
+        err_ws = np.abs(got - ws_out).max()
+        assert err_ws <= bound, f"call {call}: max err vs workspace call {err_ws:.3e} > {bound:.3e}"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(moe):
@@ -73,3 +103,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(moe):
     assert st == moe.MOE_ERR_UNSUPPORTED
     st = lib.moe_w4a16_down_combine_noalloc(p, p, p, p, 32, p, p, p, p, p, 4, E, k, 500, I, p, None)
     assert st == moe.MOE_ERR_INVALID_ARG        # H not a multiple of 32
+    st = lib.moe_w4a16_down_combine_noalloc(p, p, p, p, 16, p, p, p, p, p, 4, E, k, H, I, p, None)
+    assert st == moe.MOE_ERR_UNSUPPORTED        # group size other than 32
+    st = lib.moe_w4a16_down_combine_noalloc(p + 4, p, p, p, 32, p, p, p, p, p, 4, E, k, H, I, p, None)
+    assert st == moe.MOE_ERR_INVALID_ARG        # misaligned h

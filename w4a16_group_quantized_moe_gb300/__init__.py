@@ -29,7 +29,12 @@ MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_WAIT_TIMEOUT = 0x2
 MOE_DEVERR_BAD_METADATA = 0x4
 
-EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes",
+MOE_PATH_NONE = 0
+MOE_PATH_DECODE = 1
+MOE_PATH_TENSOR_CORE = 2
+MOE_PATH_STREAM = 3
+
+EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_step_kernel_path",
             "moe_get_device_error", "moe_topk_route", "moe_align_offsets", "moe_topk_route_align",
             "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine",
             "moe_w4a16_down_combine_noalloc", "moe_layer_workspace_bytes", "moe_w4a16_moe_layer")
@@ -63,6 +68,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_status_string.argtypes = [_I]
         lib.moe_workspace_bytes.restype = _SZ
         lib.moe_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+        lib.moe_step_kernel_path.restype = _I
+        lib.moe_step_kernel_path.argtypes = [_I, _I, _I, _I, _I]
         lib.moe_get_device_error.restype = _I
         lib.moe_get_device_error.argtypes = [_P, _SZ, ctypes.POINTER(ctypes.c_uint32), _P]
         lib.moe_topk_route.restype = _I
@@ -138,6 +145,11 @@ def new_layer_workspace(T: int, E: int, k: int, H: int, I: int, device="cuda"):
     if n == 0:
         raise MoEError("moe_layer_workspace_bytes", MOE_ERR_INVALID_ARG, "sizes rejected")
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_step_kernel_path(T: int, E: int, k: int, H: int, I: int) -> int:
+    """MOE_PATH_* of the kernels the step calls run for this shape."""
+    return int(load_library().moe_step_kernel_path(T, E, k, H, I))
 
 
 def moe_get_device_error(workspace, stream=None) -> int:

@@ -150,6 +150,16 @@ MOE_EXPORT int moe_get_device_error(void *workspace, size_t ws_bytes, uint32_t *
     return v ? MOE_ERR_DEVICE_FLAG : MOE_OK;
 }
 
+MOE_EXPORT int moe_step_kernel_path(int T, int E, int k, int H, int I) {
+    if (check_sizes(T, E, k, H, I) != MOE_OK) return MOE_PATH_NONE;
+    if (T == 0) return MOE_PATH_NONE;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess) return MOE_PATH_NONE;
+    if (decode_supported(T, E, k, H, I, di.smem_optin)) return MOE_PATH_DECODE;
+    if (tc_supported(T, E, k, H, I, di.smem_optin)) return MOE_PATH_TENSOR_CORE;
+    return MOE_PATH_STREAM;
+}
+
 MOE_EXPORT int moe_topk_route(const float *logits, int T, int E, int k, int32_t *topk_ids,
                               float *topk_w, void *stream) {
     int st = check_sizes(T, E, k, -1, -1);
@@ -246,6 +256,25 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
     return cuda_status(e);
 }
 
+namespace moe {
+// Every argument check of moe_w4a16_down_combine except the workspace's
+// (shared with the allocation-free variant, which must reject a call before
+// it touches its scratch).
+int check_down_combine_args(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
+                            const uint32_t *w2_z, int group_size, const int32_t *expert_offsets,
+                            const int32_t *sorted_pair, const int32_t *active_experts,
+                            const int32_t *num_active, const float *topk_w, int T, int E, int k, int H,
+                            int I, const uint16_t *out) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if ((st = check_group(group_size)) != MOE_OK) return st;
+    if (!all_aligned(h, w2_q, w2_s, w2_z, expert_offsets, sorted_pair, active_experts, num_active,
+                     topk_w, out))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+}  // namespace moe
+
 MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
                                       const uint32_t *w2_z, int group_size,
                                       const int32_t *expert_offsets, const int32_t *sorted_pair,
@@ -253,12 +282,9 @@ MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, c
                                       const float *topk_w, int T, int E, int k, int H, int I,
                                       uint16_t *out, void *workspace, size_t ws_bytes,
                                       void *stream) {
-    int st = check_sizes(T, E, k, H, I);
+    int st = check_down_combine_args(h, w2_q, w2_s, w2_z, group_size, expert_offsets, sorted_pair,
+                                     active_experts, num_active, topk_w, T, E, k, H, I, out);
     if (st != MOE_OK) return st;
-    if ((st = check_group(group_size)) != MOE_OK) return st;
-    if (!all_aligned(h, w2_q, w2_s, w2_z, expert_offsets, sorted_pair, active_experts, num_active,
-                     topk_w, out))
-        return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
         return MOE_ERR_WORKSPACE;
     if (T == 0) return MOE_OK;

@@ -130,6 +130,33 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {
     return v;
 }
 
+// Acquire load (gpu scope) of a counter written by other CTAs.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Nanoseconds of the GPU's global timer (for the optional phase timeline).
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One warp-level MMA, D = A.B + C: A 16x16 fp16 (row), B 16x8 fp16 (col),
+// C and D 16x8 fp32.  Fragment of lane l (group g = l / 4, t = l % 4):
+// a[0] = A[g][2t..2t+1], a[1] = A[g+8][2t..2t+1], a[2] = A[g][2t+8..2t+9],
+// a[3] = A[g+8][2t+8..2t+9]; b[0] = B[2t..2t+1][g], b[1] = B[2t+8..2t+9][g];
+// c[0..1] = C[g][2t..2t+1], c[2..3] = C[g+8][2t..2t+1].
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // Named barrier for a subset of the CTA's warps (id 0 is __syncthreads).
 __device__ inline void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
