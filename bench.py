@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--flush-mb", type=int, default=1024)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", type=int, default=0,
+                    help="also run this many steps with the decode layer's phase timestamps on "
+                         "and report their summary (decode batches only)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the secondary per-workload figures")
     ap.add_argument("--layers", type=int, default=0,
@@ -343,9 +346,7 @@ def run_reference(args, wl):
 
 
 # sources the one-launch decode layer kernel is compiled from
-DECODE_LAYER_SOURCES = ("common.cuh", "decode_common.cuh", "route.cuh", "decode_layer.cuh", "decode_layer.cu",
-                        "decode_layer_spec.cu", "decode_layer_gen16.cu", "decode_layer_gen4.cu",
-                        "decode_layer_gen1.cu")
+DECODE_LAYER_SOURCES = ("common.cuh", "route.cuh", "decode_layer.cuh", "decode_layer.cu")
 
 
 def source_digest() -> str:
@@ -489,6 +490,53 @@ def per_config_figures(moe, dev, geoms, names, sets: int):
 
 
 # grouped by weight geometry, so each geometry's weights are generated once
+TIMELINE_PHASES = ("entry", "routed_and_grouped", "first_copies_issued", "first_stage_landed",
+                   "gate_up_done", "down_inputs_ready", "down_done", "exit")
+
+
+def phase_timeline(moe, rig, steps: int, dev):
+    """Runs `steps` layer calls with the decode layer's phase timestamps on
+    (global timer, 8 per CTA) and summarises them: for each phase the median
+    and maximum over CTAs of its time since the earliest CTA entry, medians
+    over the steps; next to the CUDA-event time of the same calls (the
+    difference to the device span is the launch cost)."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    tl = torch.zeros((n_sm, 8), dtype=torch.int64, device=dev)
+    ly = rig.layers[0]
+    moe.set_diagnostics(ly.workspace, timeline=tl)
+    rows, ev_ms = [], []
+    for s in range(steps):
+        rig.stage(s)
+        tl.zero_()
+        torch.cuda._sleep(200000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(rig.stream)
+        rig.calls[0]()
+        e1.record(rig.stream)
+        torch.cuda.synchronize()
+        ev_ms.append(e0.elapsed_time(e1))
+        rows.append(tl.cpu().numpy().astype(np.float64))
+    moe.set_diagnostics(ly.workspace)
+    rig.check_errors("during the timeline steps")
+    med, mx = {}, {}
+    for i, name in enumerate(TIMELINE_PHASES):
+        per_step_med, per_step_max = [], []
+        for st in rows[1:] if len(rows) > 1 else rows:
+            t0 = st[:, 0].min()
+            v = st[:, i]
+            v = v[v > 0]
+            if len(v):
+                per_step_med.append(np.median(v - t0) / 1e3)
+                per_step_max.append(np.max(v - t0) / 1e3)
+        if per_step_med:
+            med[name] = float(np.median(per_step_med))
+            mx[name] = float(np.median(per_step_max))
+    return {"unit": "us since the first CTA entered", "steps": steps,
+            "median_over_ctas": med, "max_over_ctas": mx,
+            "event_us_median": float(np.median(ev_ms[1:] if len(ev_ms) > 1 else ev_ms) * 1e3)}
+
+
 PER_CONFIG = ("qwen4exp_decode_T1_H2560_I640_E512_k10", "qwen4exp_decode_T2_H2560_I640_E512_k10",
               "qwen4exp_decode_T4_H2560_I640_E512_k10", "qwen4exp_decode_T8_H2560_I640_E512_k10",
               "qwen4exp_prefill_T4096_H2560_I640_E512_k10", "tp4shard_decode_T2_H2560_I160_E512_k10_hot16",
@@ -581,6 +629,9 @@ def main():
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dev)
         e2e_val = whole_job_rate(world, T, e2e_steps, e2e_ms)
+        timeline = None
+        if args.timeline > 0 and T <= 8:
+            timeline = phase_timeline(moe, rig, args.timeline, dev)
         del rig
 
         per_config = None
@@ -624,6 +675,7 @@ def main():
             "layer_us_four_step_calls": med(four_ms),
             "roofline": roof,
             "per_config": per_config,
+            "timeline": timeline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,

@@ -52,7 +52,23 @@
  * must be ordered on one stream.  It also carries the device error word read
  * by moe_get_device_error.  After a device error is reported, zero the
  * workspace again before reusing it.
+ *
+ * Diagnostic words of the workspace's control block (its first 256 bytes).
+ * A zero-filled workspace selects the defaults; a caller may write them
+ * (e.g. with cudaMemcpy) between calls to test or observe the kernels:
+ *   u32 word MOE_CTRL_WAIT_POLLS  polls before an in-kernel wait on other
+ *                                 CTAs gives up (0: about one second)
+ *   u32 word MOE_CTRL_WAIT_EXTRA  added to the target of every such wait;
+ *                                 nonzero makes them unsatisfiable, so they
+ *                                 run out and report MOE_DEVERR_WAIT_TIMEOUT
+ *   u64 at word MOE_CTRL_TIMELINE device address of a buffer of 8 u64 per
+ *                                 CTA that the one-call decode layer fills
+ *                                 with global-timer stamps of its phases
+ *                                 (0: off)
  */
+#define MOE_CTRL_WAIT_POLLS 1
+#define MOE_CTRL_WAIT_EXTRA 2
+#define MOE_CTRL_TIMELINE 4
 #ifndef MOE_W4A16_H
 #define MOE_W4A16_H
 

@@ -29,6 +29,11 @@ MOE_DEVERR_BAD_EXPERT_ID = 0x1
 MOE_DEVERR_WAIT_TIMEOUT = 0x2
 MOE_DEVERR_BAD_METADATA = 0x4
 
+# diagnostic words of the workspace control block (u32 word indices)
+MOE_CTRL_WAIT_POLLS = 1
+MOE_CTRL_WAIT_EXTRA = 2
+MOE_CTRL_TIMELINE = 4
+
 MOE_PATH_NONE = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_TENSOR_CORE = 2
@@ -145,6 +150,21 @@ def new_layer_workspace(T: int, E: int, k: int, H: int, I: int, device="cuda"):
     if n == 0:
         raise MoEError("moe_layer_workspace_bytes", MOE_ERR_INVALID_ARG, "sizes rejected")
     return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def set_diagnostics(workspace, wait_polls: int = 0, wait_extra: int = 0, timeline=None):
+    """Writes the diagnostic words of a workspace's control block (stream
+    ordered): the poll limit of cross-CTA waits (0: default), an amount added
+    to every such wait's target (nonzero: the waits run out), and the device
+    buffer (int64, 8 per CTA) the one-call decode layer fills with phase
+    timestamps (None: off)."""
+    import torch
+    words = torch.zeros(6, dtype=torch.int32)
+    words[MOE_CTRL_WAIT_POLLS] = int(wait_polls)
+    words[MOE_CTRL_WAIT_EXTRA] = int(wait_extra)
+    tl = 0 if timeline is None else _dev(timeline, torch.int64, "timeline")
+    words[MOE_CTRL_TIMELINE:MOE_CTRL_TIMELINE + 2] = torch.tensor([tl], dtype=torch.int64).view(torch.int32)
+    workspace[4:24].copy_(words.view(torch.uint8)[4:24], non_blocking=False)
 
 
 def moe_step_kernel_path(T: int, E: int, k: int, H: int, I: int) -> int:

@@ -13,6 +13,11 @@ namespace moe {
 // Control block at the start of the workspace.
 constexpr size_t kCtrlBytes = 256;
 constexpr int kCtrlErrorWord = 0;     // u32: MOE_DEVERR_* bits
+// Diagnostic words of the control block (zero in a zero-filled workspace,
+// which selects the defaults); see MOE_CTRL_* in moe_w4a16.h.
+constexpr int kCtrlWaitPolls = MOE_CTRL_WAIT_POLLS;  // u32: polls before a cross-CTA wait gives up
+constexpr int kCtrlWaitExtra = MOE_CTRL_WAIT_EXTRA;  // u32: added to every cross-CTA wait target
+constexpr int kCtrlTimeline = MOE_CTRL_TIMELINE;     // u64 (words 4-5): timeline buffer address
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -33,7 +33,10 @@
 //     token in order (deterministic) and writes fp16.
 //
 // Every cross-CTA wait is bounded: on expiry it sets MOE_DEVERR_WAIT_TIMEOUT
-// in the error word and the kernel finishes without the dependent work.
+// in the error word and the kernel finishes without the dependent work.  The
+// workspace's diagnostic words set the wait limit and an offset added to the
+// wait targets (so that a test can make the waits run out), and can switch
+// on a timeline of global-timer stamps of the kernel's phases.
 // The last CTA to leave resets the per-expert counters, so consecutive calls
 // on one stream share a workspace without clearing it.
 #pragma once
@@ -49,6 +52,9 @@ constexpr int kLayerMaxPairs = 256;
 constexpr int kLayerSlots = 2;  // task buffers per warp
 constexpr int kLayerRoutePer = 32;  // logits per lane in the router (E <= 1024)
 constexpr uint32_t kPollTries = 1u << 20;  // bounded wait (about a second) for other CTAs
+
+// Stamps of the optional phase timeline (8 per CTA, global timer, ns).
+enum { kLtEntry = 0, kLtGrouped, kLtFirstIssue, kLtFirstLanded, kLtGateUpDone, kLtDownReady, kLtDownDone, kLtExit };
 
 struct LayerArgs {
     const float *logits;  // [T][E]
@@ -231,6 +237,15 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     const WarpGeom wg1 = warp_geom(RT1, 2, H), wg2 = warp_geom(RT2, 1, I);
     const int cta = blockIdx.x, NC = gridDim.x;
 
+    // diagnostics of the control block: wait limit, wait-target offset, timeline
+    const uint64_t t_entry = global_timer_ns();
+    const uint32_t polls = a.err[kCtrlWaitPolls] ? a.err[kCtrlWaitPolls] : kPollTries;
+    const uint32_t extra = a.err[kCtrlWaitExtra];
+    uint64_t *tl = reinterpret_cast<uint64_t *>(
+        *reinterpret_cast<const unsigned long long *>(a.err + kCtrlTimeline));
+    auto stamp = [&](int i) {
+        if (tl) tl[cta * 8 + i] = global_timer_ns();
+    };
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kLayerSlots; ++s) mbar_init(bars + s, 1);
@@ -283,6 +298,11 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         s_hi[slot] = g_less[p] + g_same[p];
     }
     __syncthreads();
+
+    if (tid == 0 && tl) {
+        tl[cta * 8 + kLtEntry] = t_entry;
+        stamp(kLtGrouped);
+    }
 
     // ---- 2. this CTA's shares of both task lists (weighted, contiguous)
     const int A = s_misc[0];
@@ -367,6 +387,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
 
     const int nfirst = ntask < kLayerSlots ? ntask : kLayerSlots;
     for (int i = 0; i < nfirst; ++i) issue();
+    if (tid == 0) stamp(kLtFirstIssue);
     int consumed = 0;
 
     const TaskDims td1{2 * I, H, I, P, k}, td2{H, I, H, P, k};
@@ -382,6 +403,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         if (i == n1) {
             // ---- 3. between the steps (every warp passes here once)
             __syncthreads();  // this CTA's h values are written
+            if (tid == 0) stamp(kLtGateUpDone);
             if (e1 > b1) {
                 const int lo = b1 / TPE1, hi = (e1 - 1) / TPE1;
                 for (int s = lo + tid; s <= hi; s += NTH) {
@@ -397,8 +419,8 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
                 const int lo = b2 / TPE2, hi = (e2 - 1) / TPE2;
                 for (int s = lo + tid; s <= hi; s += NTH) {
                     uint32_t it = 0;
-                    while (ld_acquire_u32(a.done + s) < (uint32_t)I && ++it < kPollTries) __nanosleep(64);
-                    if (it >= kPollTries) {
+                    while (ld_acquire_u32(a.done + s) < (uint32_t)I + extra && ++it < polls) __nanosleep(64);
+                    if (it >= polls) {
                         set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
                         s_misc[2] = 1;
                     }
@@ -421,6 +443,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
                 }
             }
             __syncthreads();
+            if (tid == 0) stamp(kLtDownReady);
             if (s_misc[2]) dead = true;
         }
         if (i == ntask) break;
@@ -436,6 +459,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             continue;
         }
         consumed = i + 1;
+        if (i == 0 && tid == 0) stamp(kLtFirstLanded);
         const uint8_t *wb = ring + (size_t)s * a.slot_bytes;
         const TaskPos tp = q0;
         q0 = q1;
@@ -492,6 +516,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     // ---- 4. publish this CTA's row counts per output block, then combine
     // this CTA's slice of blocks once every active expert's rows are in
     __syncthreads();
+    if (tid == 0) stamp(kLtDownDone);
     if (!dead) {
         for (int nb = tid; nb < nblk; nb += NTH) {
             const int c = s_blk[nb];
@@ -508,8 +533,8 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         if (s_misc[3]) break;  // an earlier wait of this CTA expired
         // every lane waits (acquire) for all rows of the block
         uint32_t it = 0;
-        while (ld_acquire_u32(a.blkctr + nb) < (uint32_t)A * 8u && ++it < kPollTries) __nanosleep(64);
-        if (__any_sync(0xffffffffu, it >= kPollTries)) {
+        while (ld_acquire_u32(a.blkctr + nb) < (uint32_t)A * 8u + extra && ++it < polls) __nanosleep(64);
+        if (__any_sync(0xffffffffu, it >= polls)) {
             if (lane == 0) {
                 set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
                 s_misc[3] = 1;
@@ -533,6 +558,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
 
     // ---- the last CTA to leave resets the per-expert counters
     __syncthreads();
+    if (tid == 0) stamp(kLtExit);
     if (tid == 0) {
         __threadfence();
         const unsigned old = atomicAdd(a.exitctr, 1u);
