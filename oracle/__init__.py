@@ -62,6 +62,19 @@ def _declare(lib):
     lib.oracle_moe_forward.argtypes = [_P, _P, _I, _I, _I, _I, _I,
                                        _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.oracle_e2m1_to_double.restype = ctypes.c_double
+    lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.oracle_dequant_nvfp4.restype = ctypes.c_double
+    lib.oracle_dequant_nvfp4.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I]
+    lib.oracle_gate_up_silu_nvfp4.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P,
+                                              _P, _P, _P, _P, _P]
+    lib.oracle_moe_token_nvfp4.argtypes = [_I, _P, _P, _I, _I, _I, _I,
+                                           _P, _P, _P, _P, _P, _P, _P]
+    lib.oracle_moe_forward_nvfp4.argtypes = [_P, _P, _I, _I, _I, _I, _I,
+                                             _P, _P, _P, _P, _P, _P,
+                                             _P, _P, _P, _P, _P, _P, _P, _P]
     return lib
 
 
@@ -199,6 +212,80 @@ def moe_forward(logits, x, w13, w2, k: int) -> dict:
     _load().oracle_moe_forward(
         _ptr(lg), _ptr(xb), T, E, k, H, I, _ptr(q13), _ptr(s13), _ptr(z13),
         _ptr(q2), _ptr(s2), _ptr(z2), _ptr(r["topk_ids"]), _ptr(r["topk_w"]),
+        _ptr(r["expert_offsets"]), _ptr(r["sorted_pair"]), _ptr(r["active_experts"]),
+        _ptr(r["num_active"]), _ptr(r["h"]), _ptr(r["out"]))
+    r["num_active"] = int(r["num_active"][0])
+    return r
+
+
+# ---------------------------------------------------------------- NVFP4
+# Weights as (codes u32 [E][N][K/8], bscale u8 [E][N][K/16], gscale f32 [E]).
+
+def e2m1_to_double(nib: int) -> float:
+    return _load().oracle_e2m1_to_double(int(nib))
+
+
+def e4m3_to_double(b: int) -> float:
+    return _load().oracle_e4m3_to_double(int(b))
+
+
+def _nv(w):
+    return _c(w[0], np.uint32), _c(w[1], np.uint8), _c(w[2], np.float32)
+
+
+def dequant_nvfp4(w, N: int, K: int, e: int, n: int, kk: int) -> float:
+    c, b, g = _nv(w)
+    return _load().oracle_dequant_nvfp4(_ptr(c), _ptr(b), _ptr(g), N, K, e, n, kk)
+
+
+def gate_up_silu_nvfp4(x, w13, meta, k: int):
+    """h [T*k, I] (float64) in sorted-pair order, NVFP4 gate/up weights."""
+    xb = half_bits(x)
+    T, H = xb.shape
+    c, b, g = _nv(w13)
+    I = c.shape[1] // 2
+    offs, sp, act, na = meta
+    na_arr = np.array([na], np.int32)
+    h = np.zeros((T * k, I), np.float64)
+    _load().oracle_gate_up_silu_nvfp4(_ptr(xb), T, H, I, k, _ptr(c), _ptr(b), _ptr(g),
+                                      _ptr(_c(offs, np.int32)), _ptr(_c(sp, np.int32)),
+                                      _ptr(_c(act, np.int32)), _ptr(na_arr), _ptr(h))
+    return h
+
+
+def moe_token_nvfp4(t: int, logits, x, w13, w2, k: int) -> np.ndarray:
+    lg = _c(logits, np.float32)
+    xb = half_bits(x)
+    E = lg.shape[1]
+    H = xb.shape[1]
+    c13, b13, g13 = _nv(w13)
+    c2, b2, g2 = _nv(w2)
+    I = c13.shape[1] // 2
+    out = np.empty(H, np.float64)
+    _load().oracle_moe_token_nvfp4(int(t), _ptr(lg), _ptr(xb), E, k, H, I,
+                                   _ptr(c13), _ptr(b13), _ptr(g13),
+                                   _ptr(c2), _ptr(b2), _ptr(g2), _ptr(out))
+    return out
+
+
+def moe_forward_nvfp4(logits, x, w13, w2, k: int) -> dict:
+    lg = _c(logits, np.float32)
+    xb = half_bits(x)
+    T, E = lg.shape
+    H = xb.shape[1]
+    c13, b13, g13 = _nv(w13)
+    c2, b2, g2 = _nv(w2)
+    I = c13.shape[1] // 2
+    P = T * k
+    r = dict(
+        topk_ids=np.empty((T, k), np.int32), topk_w=np.empty((T, k), np.float64),
+        expert_offsets=np.empty(E + 1, np.int32), sorted_pair=np.empty(P, np.int32),
+        active_experts=np.empty(E, np.int32), num_active=np.empty(1, np.int32),
+        h=np.zeros((P, I), np.float64), out=np.empty((T, H), np.float64),
+    )
+    _load().oracle_moe_forward_nvfp4(
+        _ptr(lg), _ptr(xb), T, E, k, H, I, _ptr(c13), _ptr(b13), _ptr(g13),
+        _ptr(c2), _ptr(b2), _ptr(g2), _ptr(r["topk_ids"]), _ptr(r["topk_w"]),
         _ptr(r["expert_offsets"]), _ptr(r["sorted_pair"]), _ptr(r["active_experts"]),
         _ptr(r["num_active"]), _ptr(r["h"]), _ptr(r["out"]))
     r["num_active"] = int(r["num_active"][0])

@@ -32,8 +32,21 @@
  *     w = (q - z) * s
  *   A pair is p = t*k + j: token t's j-th selected expert.
  *
+ * Second weight format (NVFP4 weights, fp16 activations).  "[Model][SM70]
+ * Adapt Qwen3.8 Flash Next NVFP4", section Implemented route, runs the
+ * checkpoint's ModelOpt NVFP4 routed experts through the W4A16 kernel with
+ * fp16 activations; the page does not restate the format, so the functions
+ * *_nvfp4 below follow its public definition: 4-bit E2M1 values, one FP8
+ * E4M3 scale per 16 consecutive elements along K, one fp32 scale per
+ * expert matrix.  Layout for one expert's W[N][K]:
+ *     codes  u32 [E][N][K/8]   value of (n, kk) = E2M1 nibble 4*(kk%8) of word [n][kk/8]
+ *     bscale u8  [E][N][K/16]  E4M3 scale of (n, kk) = bscale[n][kk/16]
+ *     gscale f32 [E]           per-expert scale
+ *     w = e2m1(code) * e4m3(bscale) * gscale
+ *
  * Parity status: every function here is pinned by the CPU test suite against
- * brute force, closed forms and invariants (see tests/test_oracle_pins.py).
+ * brute force, closed forms and invariants (see tests/test_oracle_pins.py
+ * and tests/test_oracle_nvfp4.py).
  */
 #include <math.h>
 #include <stdint.h>
@@ -300,4 +313,162 @@ ORACLE_API void oracle_moe_forward(const float *logits, const uint16_t *x,
                         sorted_pair, active_experts, num_active, h);
     oracle_down_combine(h, T, H, I, k, w2q, w2s, w2z, expert_offsets,
                         sorted_pair, active_experts, num_active, topk_w, out);
+}
+
+
+/* ---------------------------------------------------------------- NVFP4 */
+
+/* E2M1 (4 bits: sign, 2 exponent bits with bias 1, 1 mantissa bit) ->
+ * double, from the format's definition: exponent 0 is subnormal
+ * (mantissa * 2^-1 * 2^(1-1)); otherwise 2^(exp-1) * (1 + mantissa/2).  No
+ * infinities or NaN. */
+ORACLE_API double oracle_e2m1_to_double(uint8_t nib)
+{
+    int sign = (nib >> 3) & 1;
+    int expo = (nib >> 1) & 3;
+    int mant = nib & 1;
+    double v = expo == 0 ? 0.5 * mant : ldexp(1.0 + 0.5 * mant, expo - 1);
+    return sign ? -v : v;
+}
+
+/* FP8 E4M3 (sign, 4 exponent bits with bias 7, 3 mantissa bits, the
+ * variant without infinities) -> double: exponent 0 is subnormal
+ * (mantissa/8 * 2^-6); the all-ones exponent with all-ones mantissa is NaN;
+ * otherwise 2^(exp-7) * (1 + mantissa/8). */
+ORACLE_API double oracle_e4m3_to_double(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int expo = (b >> 3) & 15;
+    int mant = b & 7;
+    double v;
+    if (expo == 15 && mant == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)mant / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)mant / 8.0, expo - 7);
+    return sign ? -v : v;
+}
+
+/* Dequantised NVFP4 weight of element (n, kk) of expert e's W[N][K]. */
+ORACLE_API double oracle_dequant_nvfp4(const uint32_t *codes, const uint8_t *bscale,
+                                       const float *gscale, int N, int K,
+                                       int e, int n, int kk)
+{
+    size_t word = ((size_t)e * N + n) * (K / 8) + kk / 8;
+    uint8_t nib = (uint8_t)((codes[word] >> (4 * (kk % 8))) & 0xfu);
+    double bs = oracle_e4m3_to_double(bscale[((size_t)e * N + n) * (K / 16) + kk / 16]);
+    return oracle_e2m1_to_double(nib) * bs * (double)gscale[e];
+}
+
+static void expert_gate_up_nvfp4(const uint16_t *xrow, int H, int I,
+                                 const uint32_t *c13, const uint8_t *b13,
+                                 const float *g13, int e, double *hrow)
+{
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+            double xv = oracle_half_to_double(xrow[c]);
+            g += xv * oracle_dequant_nvfp4(c13, b13, g13, 2 * I, H, e, i, c);
+            u += xv * oracle_dequant_nvfp4(c13, b13, g13, 2 * I, H, e, I + i, c);
+        }
+        hrow[i] = u * silu(g);
+    }
+}
+
+static void expert_down_nvfp4(const double *hrow, int H, int I,
+                              const uint32_t *c2, const uint8_t *b2,
+                              const float *g2, int e, double *yrow)
+{
+    for (int n = 0; n < H; ++n) {
+        double y = 0.0;
+        for (int i = 0; i < I; ++i)
+            y += hrow[i] * oracle_dequant_nvfp4(c2, b2, g2, H, I, e, n, i);
+        yrow[n] = y;
+    }
+}
+
+/* Step 3 with NVFP4 weights (as oracle_gate_up_silu). */
+ORACLE_API void oracle_gate_up_silu_nvfp4(const uint16_t *x, int T, int H, int I, int k,
+                                          const uint32_t *c13, const uint8_t *b13,
+                                          const float *g13,
+                                          const int32_t *expert_offsets,
+                                          const int32_t *sorted_pair,
+                                          const int32_t *active_experts,
+                                          const int32_t *num_active, double *h)
+{
+    (void)T;
+    for (int a = 0; a < num_active[0]; ++a) {
+        int e = active_experts[a];
+        for (int r = expert_offsets[e]; r < expert_offsets[e + 1]; ++r) {
+            int t = sorted_pair[r] / k;
+            expert_gate_up_nvfp4(x + (size_t)t * H, H, I, c13, b13, g13, e,
+                                 h + (size_t)r * I);
+        }
+    }
+}
+
+/* The layer for a single token with NVFP4 weights (as oracle_moe_token). */
+ORACLE_API void oracle_moe_token_nvfp4(int t, const float *logits, const uint16_t *x,
+                                       int E, int k, int H, int I,
+                                       const uint32_t *c13, const uint8_t *b13,
+                                       const float *g13,
+                                       const uint32_t *c2, const uint8_t *b2,
+                                       const float *g2, double *out_row)
+{
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+    double *w = (double *)malloc(sizeof(double) * (size_t)k);
+    double *hrow = (double *)malloc(sizeof(double) * (size_t)I);
+    double *yrow = (double *)malloc(sizeof(double) * (size_t)H);
+    oracle_route(logits + (size_t)t * E, 1, E, k, ids, w);
+    for (int n = 0; n < H; ++n) out_row[n] = 0.0;
+    for (int j = 0; j < k; ++j) {
+        expert_gate_up_nvfp4(x + (size_t)t * H, H, I, c13, b13, g13, ids[j], hrow);
+        expert_down_nvfp4(hrow, H, I, c2, b2, g2, ids[j], yrow);
+        for (int n = 0; n < H; ++n) out_row[n] += w[j] * yrow[n];
+    }
+    free(ids);
+    free(w);
+    free(hrow);
+    free(yrow);
+}
+
+/* The four steps over a batch with NVFP4 weights (as oracle_moe_forward):
+ * routing and grouping are those of the W4A16 layer; steps 3 and 4 read
+ * the NVFP4 matrices. */
+ORACLE_API void oracle_moe_forward_nvfp4(const float *logits, const uint16_t *x,
+                                         int T, int E, int k, int H, int I,
+                                         const uint32_t *c13, const uint8_t *b13,
+                                         const float *g13,
+                                         const uint32_t *c2, const uint8_t *b2,
+                                         const float *g2,
+                                         int32_t *topk_ids, double *topk_w,
+                                         int32_t *expert_offsets, int32_t *sorted_pair,
+                                         int32_t *active_experts, int32_t *num_active,
+                                         double *h, double *out)
+{
+    int P = T * k;
+    oracle_route(logits, T, E, k, topk_ids, topk_w);
+    oracle_align(topk_ids, T, E, k, expert_offsets, sorted_pair, active_experts,
+                 num_active);
+    oracle_gate_up_silu_nvfp4(x, T, H, I, k, c13, b13, g13, expert_offsets,
+                              sorted_pair, active_experts, num_active, h);
+    double *y = (double *)malloc(sizeof(double) * (size_t)P * H);
+    int *row_of_pair = (int *)malloc(sizeof(int) * (size_t)P);
+    for (int a = 0; a < num_active[0]; ++a) {
+        int e = active_experts[a];
+        for (int r = expert_offsets[e]; r < expert_offsets[e + 1]; ++r) {
+            expert_down_nvfp4(h + (size_t)r * I, H, I, c2, b2, g2, e, y + (size_t)r * H);
+            row_of_pair[sorted_pair[r]] = r;
+        }
+    }
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int j = 0; j < k; ++j)
+                acc += topk_w[(size_t)t * k + j] * y[(size_t)row_of_pair[t * k + j] * H + n];
+            out[(size_t)t * H + n] = acc;
+        }
+    free(y);
+    free(row_of_pair);
 }

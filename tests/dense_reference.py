@@ -26,6 +26,30 @@ def unpack_matrix(qweight, scales, qzeros):
     return (q - zf) * sf
 
 
+# E2M1 values of the 16 codes (sign, 2 exponent bits, 1 mantissa bit), as
+# tabulated in the OCP Microscaling Formats specification (FP4 E2M1).
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                        -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def e4m3_values():
+    """FP8 E4M3 value of each of the 256 bytes, decoded by PyTorch's
+    float8_e4m3fn dtype (a library routine, not the oracle's decoder)."""
+    import torch
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def unpack_matrix_nvfp4(codes, bscale, gscale):
+    """Dense [E][N][K] float64 weights from the NVFP4 layout."""
+    E, N, KW = codes.shape
+    K = KW * 8
+    shifts = (4 * np.arange(8, dtype=np.uint32))
+    q = ((codes[..., None] >> shifts) & np.uint32(0xF)).reshape(E, N, K)
+    v = E2M1_VALUES[q]
+    bs = e4m3_values()[bscale]                                   # [E][N][K/16]
+    return v * np.repeat(bs, 16, axis=2) * np.asarray(gscale, np.float64)[:, None, None]
+
+
 def route_dense(logits, k):
     """Full softmax over E, rank by (logit desc, index asc), keep k, renormalise."""
     T, E = logits.shape
@@ -45,10 +69,10 @@ def silu(v):
     return v / (1.0 + np.exp(-v))
 
 
-def moe_dense(logits, x, w13, w2, k):
+def moe_dense(logits, x, w13, w2, k, unpack=unpack_matrix):
     """out [T][H], h_dense [E][T][I], gate [T][E] by dense evaluation."""
-    W13 = unpack_matrix(*w13)                 # [E][2I][H]
-    W2 = unpack_matrix(*w2)                   # [E][H][I]
+    W13 = unpack(*w13)                        # [E][2I][H]
+    W2 = unpack(*w2)                          # [E][H][I]
     E, twoI, H = W13.shape
     I = twoI // 2
     T = logits.shape[0]

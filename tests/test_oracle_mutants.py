@@ -7,6 +7,7 @@ import subprocess
 import pytest
 
 import oracle
+from tests import test_oracle_nvfp4 as nv
 from tests import test_oracle_pins as pins
 from w4a16_group_quantized_moe_gb300 import inputs
 
@@ -34,6 +35,22 @@ MUTANTS = [
      "for (int p = P - 1; p >= 0; --p)\n            if (topk_ids[p] == e)"),
     ("last group of K dropped", "for (int kk = 0; kk < H; ++kk) {",
      "for (int kk = 0; kk < H - 32; ++kk) {"),
+]
+
+# planted mistakes in the NVFP4 functions, checked by the NVFP4 pins
+NVFP4_MUTANTS = [
+    ("e2m1 sign dropped", "return sign ? -v : v;\n}\n\n/* FP8 E4M3", "return v;\n}\n\n/* FP8 E4M3"),
+    ("e2m1 subnormal as normal", "double v = expo == 0 ? 0.5 * mant : ldexp(1.0 + 0.5 * mant, expo - 1);",
+     "double v = ldexp(1.0 + 0.5 * mant, expo - 1);"),
+    ("e4m3 bias off by one", "v = ldexp(1.0 + (double)mant / 8.0, expo - 7);",
+     "v = ldexp(1.0 + (double)mant / 8.0, expo - 8);"),
+    ("block of 32 instead of 16", "bscale[((size_t)e * N + n) * (K / 16) + kk / 16]",
+     "bscale[((size_t)e * N + n) * (K / 16) + kk / 32]"),
+    ("per-expert scale dropped", "return oracle_e2m1_to_double(nib) * bs * (double)gscale[e];",
+     "return oracle_e2m1_to_double(nib) * bs;"),
+    ("nvfp4 gate used for up", "u += xv * oracle_dequant_nvfp4(c13, b13, g13, 2 * I, H, e, I + i, c);",
+     "u += xv * oracle_dequant_nvfp4(c13, b13, g13, 2 * I, H, e, i, c);"),
+    ("nvfp4 silu dropped", "hrow[i] = u * silu(g);", "hrow[i] = u * g;"),
 ]
 
 CHECKS = [
@@ -66,7 +83,36 @@ def test_planted_mistake_is_caught(tmp_path, name, orig, mut):
     assert caught, f"no pin rejects the planted mistake '{name}'"
 
 
+NVFP4_CHECKS = [
+    nv.test_e2m1_matches_the_specification_table,
+    nv.test_e4m3_matches_torch_for_every_byte,
+    nv.test_dequant_hand_derived_word,
+    nv.test_dequant_uses_the_block_of_sixteen,
+    lambda m: nv.test_layer_matches_dense_brute_force(m, nv.SHAPES[0]),
+    nv.test_layer_constant_closed_form,
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", NVFP4_MUTANTS, ids=[m[0] for m in NVFP4_MUTANTS])
+def test_planted_nvfp4_mistake_is_caught(tmp_path, name, orig, mut):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor for '{name}' not unique"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(orig, mut))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-fvisibility=hidden", str(mpath), "-o", str(lib), "-lm"])
+    caught = []
+    with oracle.using_library(str(lib)):
+        for check in NVFP4_CHECKS:
+            try:
+                check(oracle)
+            except AssertionError:
+                caught.append(check)
+    assert caught, f"no pin rejects the planted mistake '{name}'"
+
+
 def test_unmutated_source_passes_every_check():
-    for check in CHECKS:
+    for check in CHECKS + NVFP4_CHECKS:
         check(oracle)
     assert inputs.TINY.shape.k == 2

@@ -94,6 +94,23 @@ def make_weights(E: int, H: int, I: int, seed: int = 0):
     return w13, w2
 
 
+def make_weights_nvfp4(E: int, H: int, I: int, seed: int = 0):
+    """(w13, w2) in the NVFP4 layout, each a tuple (codes u32 [E][N][K/8],
+    bscale u8 [E][N][K/16], gscale f32 [E]).  Codes: uniformly random words
+    (eight independent E2M1 codes, both signs); block scales: FP8 E4M3 bytes
+    drawn uniformly from 0x30-0x3F (0.5 to 1.875); per-expert scales
+    ~ U[0.005, 0.02], so weights span the same range as the W4A16 ones."""
+    if H % 32 or I % 32:
+        raise ValueError("H and I must be multiples of 32")
+
+    def mat(tag, N, K):
+        codes = _words(_rng(seed, tag), (E, N, K // 8))
+        bs = _rng(seed, tag + 1).integers(0x30, 0x40, size=(E, N, K // 16), dtype=np.uint8)
+        gs = (np.float32(0.005) + np.float32(0.015) * _rng(seed, tag + 2).random(E, dtype=np.float32))
+        return codes, bs, gs.astype(np.float32)
+    return mat(31, 2 * I, H), mat(41, H, I)
+
+
 def make_activations(T: int, H: int, E: int, seed: int = 0, hot_experts=(), hot_bias=0.0):
     """(logits f32 [T,E], x f16 [T,H])."""
     logits = _rng(seed, 1).standard_normal((T, E), dtype=np.float32)
@@ -117,6 +134,14 @@ def random_topk_ids(T: int, E: int, k: int, seed: int = 0) -> np.ndarray:
     grouping step on its own)."""
     rng = _rng(seed, 3)
     return np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+def bytes_per_expert_nvfp4(H: int, I: int) -> dict:
+    """Bytes of one expert's NVFP4 weights (codes + E4M3 block scales +
+    the fp32 per-expert scale)."""
+    def mat(N, K):
+        return N * K // 2 + N * (K // 16) + 4
+    return {"w13": mat(2 * I, H), "w2": mat(H, I)}
 
 
 def bytes_per_expert(H: int, I: int) -> dict:
