@@ -75,6 +75,13 @@ def _declare(lib):
     lib.oracle_moe_forward_nvfp4.argtypes = [_P, _P, _I, _I, _I, _I, _I,
                                              _P, _P, _P, _P, _P, _P,
                                              _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.oracle_router_logits.argtypes = [_P, _P, _I, _I, _I, _P]
+    for f in (lib.oracle_awq_q, lib.oracle_awq_z):
+        f.restype = _I
+        f.argtypes = [_P, _I, _I, _I, _I, _I]
+    lib.oracle_awq_s.restype = ctypes.c_uint16
+    lib.oracle_awq_s.argtypes = [_P, _I, _I, _I, _I, _I]
+    lib.oracle_awq_import.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _I, _I]
     return lib
 
 
@@ -290,3 +297,49 @@ def moe_forward_nvfp4(logits, x, w13, w2, k: int) -> dict:
         _ptr(r["num_active"]), _ptr(r["h"]), _ptr(r["out"]))
     r["num_active"] = int(r["num_active"][0])
     return r
+
+
+# ---------------------------------------------------------------- router logits
+def router_logits(x, wr) -> np.ndarray:
+    """logits [T, E] (float64) = x [T, H] (fp16) times wr [E, H] (fp16) transposed."""
+    xb, wb = half_bits(x), half_bits(wr)
+    T, H = xb.shape
+    E = wb.shape[0]
+    if wb.shape[1] != H:
+        raise ValueError("router matrix must be [E, H]")
+    out = np.empty((T, E), np.float64)
+    _load().oracle_router_logits(_ptr(xb), _ptr(wb), T, E, H, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------- AWQ import
+# AWQ layer = (qweight u32 [E][K][N/8], qzeros u32 [E][K/32][N/8], scales f16 [E][K/32][N]).
+
+def awq_element(awq, K: int, N: int, e: int, n: int, kk: int):
+    """(q, z, scale bits) of element (n, kk) of expert e's AWQ layer."""
+    aq, az, as_ = _c(awq[0], np.uint32), _c(awq[1], np.uint32), half_bits(awq[2])
+    lib = _load()
+    return (lib.oracle_awq_q(_ptr(aq), K, N, e, n, kk), lib.oracle_awq_z(_ptr(az), K, N, e, n, kk),
+            lib.oracle_awq_s(_ptr(as_), K, N, e, n, kk))
+
+
+def awq_import(awq, dst, row0: int = 0):
+    """Writes the AWQ layer into rows [row0, row0+N) of dst = (qweight,
+    scales, qzeros) in the layer's layout, in place; returns dst."""
+    aq, az, as_ = _c(awq[0], np.uint32), _c(awq[1], np.uint32), half_bits(awq[2])
+    E, K, N8 = aq.shape
+    N = N8 * 8
+    q, s, z = dst
+    for a, dt in ((q, np.uint32), (z, np.uint32)):
+        if a.dtype != dt or not a.flags.c_contiguous:
+            raise TypeError("destination must be contiguous uint32")
+    if s.dtype != np.float16 or not s.flags.c_contiguous:
+        raise TypeError("destination scales must be contiguous float16")
+    Ndst = q.shape[1]
+    if q.shape != (E, Ndst, K // 8) or s.shape != (E, Ndst, K // 32) or z.shape != (E, Ndst // 8, K // 32):
+        raise ValueError("destination shapes do not match")
+    if row0 % 8 or row0 + N > Ndst:
+        raise ValueError("row0 must be a multiple of 8 and the rows must fit")
+    _load().oracle_awq_import(_ptr(aq), _ptr(az), _ptr(as_), E, K, N, _ptr(q), _ptr(s.view(np.uint16)),
+                              _ptr(z), Ndst, row0)
+    return dst

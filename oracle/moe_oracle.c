@@ -472,3 +472,88 @@ ORACLE_API void oracle_moe_forward_nvfp4(const float *logits, const uint16_t *x,
     free(y);
     free(row_of_pair);
 }
+
+/* ---------------------------------------------------------------- router logits
+ * The step ahead of routing.  The pages treat the router's fp32 logits as
+ * given; the model's gate is a bias-free linear map from the hidden state to
+ * one score per expert, so
+ *     logits[t][e] = sum over h of x[t][h] * wr[e][h]
+ * with x binary16 [T][H] and the router matrix wr binary16 [E][H] (one row
+ * per expert, the layout of a linear layer's weight), evaluated in double. */
+ORACLE_API void oracle_router_logits(const uint16_t *x, const uint16_t *wr,
+                                     int T, int E, int H, double *logits)
+{
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int c = 0; c < H; ++c)
+                acc += oracle_half_to_double(x[(size_t)t * H + c]) *
+                       oracle_half_to_double(wr[(size_t)e * H + c]);
+            logits[(size_t)t * E + e] = acc;
+        }
+}
+
+/* ---------------------------------------------------------------- AWQ import
+ * The grouped-decode work reads AWQ g32 checkpoints ("[Model][SM70] Support
+ * Qwen3.8 Flash Next with PLE offload", section Purpose, names the AWQ g32
+ * metadata adapter).  The pages do not restate the checkpoint layout; these
+ * functions follow the public AWQ "GEMM" packing of one linear layer with
+ * input size K and output size N:
+ *     qweight u32  [K][N/8]    nibble i of word [kk][c] is q of output column 8c + ORDER[i]
+ *     qzeros  u32  [K/32][N/8] nibble i of word [g][c]  is z of output column 8c + ORDER[i]
+ *     scales  f16  [K/32][N]
+ *     ORDER = (0, 2, 4, 6, 1, 3, 5, 7), w = (q - z) * s as in the layer.
+ * Experts are stacked along a leading E axis.  The import writes the same
+ * (q, z, s) into the layer's layout (header of this file) at rows
+ * [row0, row0 + N) of a destination with Ndst rows per expert, so that the
+ * gate and up layers of an expert land in the two halves of W13. */
+static const int awq_column_of_nibble[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+/* The nibble slot (0..7) of a word that holds output column n. */
+static int awq_slot_of_column(int n)
+{
+    for (int i = 0; i < 8; ++i)
+        if (awq_column_of_nibble[i] == n % 8) return i;
+    return -1;
+}
+
+ORACLE_API int oracle_awq_q(const uint32_t *aq, int K, int N, int e, int n, int kk)
+{
+    uint32_t w = aq[((size_t)e * K + kk) * (N / 8) + n / 8];
+    return (int)((w >> (4 * awq_slot_of_column(n))) & 0xfu);
+}
+
+ORACLE_API int oracle_awq_z(const uint32_t *az, int K, int N, int e, int n, int kk)
+{
+    uint32_t w = az[((size_t)e * (K / 32) + kk / 32) * (N / 8) + n / 8];
+    return (int)((w >> (4 * awq_slot_of_column(n))) & 0xfu);
+}
+
+ORACLE_API uint16_t oracle_awq_s(const uint16_t *as, int K, int N, int e, int n, int kk)
+{
+    return as[((size_t)e * (K / 32) + kk / 32) * N + n];
+}
+
+static void put_nibble(uint32_t *word, int slot, int v)
+{
+    *word = (*word & ~(0xfu << (4 * slot))) | ((uint32_t)v << (4 * slot));
+}
+
+/* Element by element: every (e, n, kk) of the AWQ matrices is read with the
+ * accessors above and written to its place in the layer's layout. */
+ORACLE_API void oracle_awq_import(const uint32_t *aq, const uint32_t *az, const uint16_t *as,
+                                  int E, int K, int N, uint32_t *qweight, uint16_t *scales,
+                                  uint32_t *qzeros, int Ndst, int row0)
+{
+    for (int e = 0; e < E; ++e)
+        for (int n = 0; n < N; ++n) {
+            int r = row0 + n;
+            for (int kk = 0; kk < K; ++kk) {
+                put_nibble(&qweight[((size_t)e * Ndst + r) * (K / 8) + kk / 8], kk % 8,
+                           oracle_awq_q(aq, K, N, e, n, kk));
+                put_nibble(&qzeros[((size_t)e * (Ndst / 8) + r / 8) * (K / 32) + kk / 32], r % 8,
+                           oracle_awq_z(az, K, N, e, n, kk));
+                scales[((size_t)e * Ndst + r) * (K / 32) + kk / 32] = oracle_awq_s(as, K, N, e, n, kk);
+            }
+        }
+}

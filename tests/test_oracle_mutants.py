@@ -9,6 +9,7 @@ import pytest
 import oracle
 from tests import test_oracle_nvfp4 as nv
 from tests import test_oracle_pins as pins
+from tests import test_oracle_router_awq as ra
 from w4a16_group_quantized_moe_gb300 import inputs
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
@@ -112,7 +113,56 @@ def test_planted_nvfp4_mistake_is_caught(tmp_path, name, orig, mut):
     assert caught, f"no pin rejects the planted mistake '{name}'"
 
 
+# planted mistakes in the router-logits product and the AWQ import
+RA_MUTANTS = [
+    ("router matrix read transposed", "oracle_half_to_double(wr[(size_t)e * H + c]);",
+     "oracle_half_to_double(wr[(size_t)c * E + e]);"),
+    ("router last term dropped", "for (int c = 0; c < H; ++c)\n                acc +=",
+     "for (int c = 0; c < H - 1; ++c)\n                acc +="),
+    ("awq natural nibble order", "{0, 2, 4, 6, 1, 3, 5, 7};", "{0, 1, 2, 3, 4, 5, 6, 7};"),
+    ("awq qweight indexed as [N/8][K]", "aq[((size_t)e * K + kk) * (N / 8) + n / 8];",
+     "aq[((size_t)e * (N / 8) + n / 8) * K + kk];"),
+    ("awq zero word of column ignored", "az[((size_t)e * (K / 32) + kk / 32) * (N / 8) + n / 8];",
+     "az[((size_t)e * (K / 32) + kk / 32) * (N / 8)];"),
+    ("awq scales not transposed", "as[((size_t)e * (K / 32) + kk / 32) * N + n];",
+     "as[((size_t)e * N + n) * (K / 32) + kk / 32];"),
+    ("imported zero nibble by column of K", "r % 8,\n                           oracle_awq_z",
+     "kk % 8,\n                           oracle_awq_z"),
+    ("imported rows not offset", "int r = row0 + n;", "int r = n;"),
+]
+
+RA_CHECKS = [
+    ra.test_router_logits_exact_on_tiny_input,
+    ra.test_router_logits_one_hot_picks_a_column,
+    ra.test_router_logits_match_library_product,
+    ra.test_awq_order_word_gives_column_index,
+    ra.test_awq_single_nibbles_land_where_derived,
+    ra.test_awq_scales_are_transposed,
+    ra.test_awq_import_preserves_every_dequantised_weight,
+    ra.test_awq_import_into_upper_half_leaves_lower_half,
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", RA_MUTANTS, ids=[m[0] for m in RA_MUTANTS])
+def test_planted_router_awq_mistake_is_caught(tmp_path, name, orig, mut):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor for '{name}' not unique"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(orig, mut))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-fvisibility=hidden", str(mpath), "-o", str(lib), "-lm"])
+    caught = []
+    with oracle.using_library(str(lib)):
+        for check in RA_CHECKS:
+            try:
+                check(oracle)
+            except (AssertionError, IndexError, ValueError):
+                caught.append(check)
+    assert caught, f"no pin rejects the planted mistake '{name}'"
+
+
 def test_unmutated_source_passes_every_check():
-    for check in CHECKS + NVFP4_CHECKS:
+    for check in CHECKS + NVFP4_CHECKS + RA_CHECKS:
         check(oracle)
     assert inputs.TINY.shape.k == 2
