@@ -239,6 +239,47 @@ int moe_w4a16_moe_layer(const float *logits, const uint16_t *x,
                         int32_t *topk_ids, float *topk_w, uint16_t *out,
                         void *workspace, size_t ws_bytes, void *stream);
 
+/* ---- Second weight format: NVFP4 weights with fp16 activations.
+ * "[Model][SM70] Adapt Qwen3.8 Flash Next NVFP4", section Implemented route,
+ * runs the checkpoint's ModelOpt NVFP4 routed experts through the W4A16
+ * kernel with fp16 activations (the "A16" route).  The format, as publicly
+ * defined, for one expert's matrix W[N][K]:
+ *   codes  u32 [N][K/8]  : E2M1 value of (n, kk) = nibble 4*(kk%8) of word [n][kk/8]
+ *                          (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa)
+ *   bscale u8  [N][K/16] : FP8 E4M3 scale of (n, kk) = bscale[n][kk/16]
+ *   gscale f32 per expert: scale of the whole matrix
+ *   w(n, kk) = e2m1(code) * e4m3(bscale) * gscale[e]
+ * Experts are stacked as for W4A16 (codes [E][N][K/8], bscale [E][N][K/16],
+ * gscale [E]).  The three calls below take the place of steps 3, 4 and the
+ * one-call layer; routing, grouping, workspace sizes and rules, error codes
+ * and results are as for the W4A16 calls.  Arithmetic: e2m1 values times
+ * activations in fp16 within each 16-element block, scaled by the block's
+ * E4M3 scale and the expert's scale in fp32 (decode kernels), or the MMA
+ * operand e2m1 * e4m3 in fp16 (exact) with fp32 accumulation and the
+ * expert's scale applied to the accumulator (tensor-core kernels).  Shapes
+ * that neither the decode kernels nor the tensor-core kernels take (the
+ * staged stream band) return MOE_ERR_UNSUPPORTED before any launch.
+ * Scale products |e4m3 * gscale| and activations must keep each block's fp16
+ * partial sum finite. */
+int moe_nvfp4_gate_up_silu(const uint16_t *x, const uint32_t *w13_codes, const uint8_t *w13_bscale,
+                           const float *w13_gscale, const int32_t *expert_offsets,
+                           const int32_t *sorted_pair, const int32_t *active_experts,
+                           const int32_t *num_active, int T, int E, int k, int H, int I, uint16_t *h,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+int moe_nvfp4_down_combine(const uint16_t *h, const uint32_t *w2_codes, const uint8_t *w2_bscale,
+                           const float *w2_gscale, const int32_t *expert_offsets,
+                           const int32_t *sorted_pair, const int32_t *active_experts,
+                           const int32_t *num_active, const float *topk_w, int T, int E, int k, int H,
+                           int I, uint16_t *out, void *workspace, size_t ws_bytes, void *stream);
+
+/* The whole layer with NVFP4 weights (workspace: moe_layer_workspace_bytes). */
+int moe_nvfp4_moe_layer(const float *logits, const uint16_t *x, const uint32_t *w13_codes,
+                        const uint8_t *w13_bscale, const float *w13_gscale, const uint32_t *w2_codes,
+                        const uint8_t *w2_bscale, const float *w2_gscale, int T, int E, int k, int H,
+                        int I, int32_t *topk_ids, float *topk_w, uint16_t *out, void *workspace,
+                        size_t ws_bytes, void *stream);
+
 /* Step 4 for callers that cannot allocate device memory.  The paper has no
  * counterpart: this is a convenience of this library.  Some callers are not
  * allowed to call cudaMalloc -- an engine that plans all device memory

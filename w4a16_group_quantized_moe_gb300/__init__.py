@@ -42,7 +42,8 @@ MOE_PATH_STREAM = 3
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_step_kernel_path",
             "moe_get_device_error", "moe_topk_route", "moe_align_offsets", "moe_topk_route_align",
             "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine",
-            "moe_w4a16_down_combine_noalloc", "moe_layer_workspace_bytes", "moe_w4a16_moe_layer")
+            "moe_w4a16_down_combine_noalloc", "moe_layer_workspace_bytes", "moe_w4a16_moe_layer",
+            "moe_nvfp4_gate_up_silu", "moe_nvfp4_down_combine", "moe_nvfp4_moe_layer")
 
 _lock = threading.Lock()
 _lib = None
@@ -96,6 +97,15 @@ def load_library(path: str = LIB_PATH):
         lib.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
         lib.moe_w4a16_moe_layer.restype = _I
         lib.moe_w4a16_moe_layer.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                            _P, _P, _P, _P, _SZ, _P]
+        lib.moe_nvfp4_gate_up_silu.restype = _I
+        lib.moe_nvfp4_gate_up_silu.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P,
+                                               _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+        lib.moe_nvfp4_down_combine.restype = _I
+        lib.moe_nvfp4_down_combine.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+        lib.moe_nvfp4_moe_layer.restype = _I
+        lib.moe_nvfp4_moe_layer.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                             _P, _P, _P, _P, _SZ, _P]
         _lib = lib
         return lib
@@ -327,6 +337,81 @@ def moe_w4a16_moe_layer(logits, x, w13, w2, k: int, workspace, topk_ids=None, to
     return out, topk_ids, topk_w
 
 
+def moe_nvfp4_gate_up_silu(x, w13, meta, k: int, workspace, h=None, stream=None):
+    """h[T*k, I] (fp16, sorted-row order).  w13 = (codes, bscale, gscale) NVFP4."""
+    import torch
+    c, b, g = w13
+    T, H = x.shape
+    E, twoI, _ = c.shape
+    I = twoI // 2
+    offs, sp, act, na = meta
+    if h is None:
+        h = torch.empty((T * k, I), dtype=torch.float16, device=x.device)
+    _check("moe_nvfp4_gate_up_silu", load_library().moe_nvfp4_gate_up_silu(
+        _dev(x, torch.float16, "x"), _dev(c, torch.int32, "w13_codes"), _dev(b, torch.uint8, "w13_bscale"),
+        _dev(g, torch.float32, "w13_gscale"), _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), T, E, k, H, I, _dev(h, torch.float16, "h"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return h
+
+
+def moe_nvfp4_down_combine(h, w2, meta, topk_w, workspace, out=None, stream=None):
+    """out[T, H] (fp16).  w2 = (codes, bscale, gscale) NVFP4."""
+    import torch
+    c, b, g = w2
+    E, H, _ = c.shape
+    T, k = topk_w.shape
+    I = h.shape[1]
+    offs, sp, act, na = meta
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float16, device=h.device)
+    _check("moe_nvfp4_down_combine", load_library().moe_nvfp4_down_combine(
+        _dev(h, torch.float16, "h"), _dev(c, torch.int32, "w2_codes"), _dev(b, torch.uint8, "w2_bscale"),
+        _dev(g, torch.float32, "w2_gscale"), _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), _dev(topk_w, torch.float32, "topk_w"),
+        T, E, k, H, I, _dev(out, torch.float16, "out"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return out
+
+
+def moe_nvfp4_moe_layer(logits, x, w13, w2, k: int, workspace, topk_ids=None, topk_w=None,
+                        out=None, stream=None):
+    """The whole layer with NVFP4 weights in one C call; (out, topk_ids, topk_w)."""
+    import torch
+    T, E = logits.shape
+    H = x.shape[1]
+    I = w2[0].shape[2] * 8
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float16, device=logits.device)
+    c13, b13, g13 = w13
+    c2, b2, g2 = w2
+    _check("moe_nvfp4_moe_layer", load_library().moe_nvfp4_moe_layer(
+        _dev(logits, torch.float32, "logits"), _dev(x, torch.float16, "x"),
+        _dev(c13, torch.int32, "w13_codes"), _dev(b13, torch.uint8, "w13_bscale"),
+        _dev(g13, torch.float32, "w13_gscale"), _dev(c2, torch.int32, "w2_codes"),
+        _dev(b2, torch.uint8, "w2_bscale"), _dev(g2, torch.float32, "w2_gscale"),
+        T, E, k, H, I, _dev(topk_ids, torch.int32, "topk_ids"), _dev(topk_w, torch.float32, "topk_w"),
+        _dev(out, torch.float16, "out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
+    return out, topk_ids, topk_w
+
+
+def to_device_weights_nvfp4(w, device="cuda"):
+    """(codes u32, bscale u8, gscale f32) numpy arrays -> CUDA tensors (codes viewed as int32)."""
+    import numpy as np
+    import torch
+    c, b, g = w
+    return (torch.from_numpy(np.ascontiguousarray(c).view(np.int32)).to(device),
+            torch.from_numpy(np.ascontiguousarray(b)).to(device),
+            torch.from_numpy(np.ascontiguousarray(g, dtype=np.float32)).to(device))
+
+
 def to_device_weights(w, device="cuda"):
     """(qweight, scales, qzeros) numpy arrays -> CUDA tensors (u32 viewed as int32)."""
     import numpy as np
@@ -413,3 +498,56 @@ class MoELayer:
                 call(lib.moe_align_offsets, "moe_align_offsets", a_align),
                 call(lib.moe_w4a16_gate_up_silu, "moe_w4a16_gate_up_silu", a_gu),
                 call(lib.moe_w4a16_down_combine, "moe_w4a16_down_combine", a_dn))
+
+
+class MoELayerNvfp4(MoELayer):
+    """MoELayer with NVFP4 weights: w13 / w2 = (codes, bscale, gscale) CUDA
+    tensors (to_device_weights_nvfp4); routing and grouping as for W4A16."""
+
+    def forward(self, logits, x, stream=None):
+        moe_topk_route(logits, self.k, self.topk_ids, self.topk_w, stream=stream)
+        moe_align_offsets(self.topk_ids, self.E, self.workspace, out=self.meta, stream=stream)
+        moe_nvfp4_gate_up_silu(x, self.w13, self.meta, self.k, self.workspace, h=self.h, stream=stream)
+        moe_nvfp4_down_combine(self.h, self.w2, self.meta, self.topk_w, self.workspace,
+                               out=self.out, stream=stream)
+        return self.out
+
+    def forward_layer(self, logits, x, stream=None):
+        moe_nvfp4_moe_layer(logits, x, self.w13, self.w2, self.k, self.workspace,
+                            topk_ids=self.topk_ids, topk_w=self.topk_w, out=self.out, stream=stream)
+        return self.out
+
+    def bind(self, logits, x, stream=None):
+        """(route_align, gate_up, down) zero-argument callables, one C call
+        each; sets self.layer_call (the whole layer in one call)."""
+        import torch
+        lib = load_library()
+        st = _stream(stream)
+        T, E, k, H, I = self.T, self.E, self.k, self.H, self.I
+        offs, sp, act, na = (t.data_ptr() for t in self.meta)
+        ws, wsb = self.workspace.data_ptr(), self.workspace.numel()
+        _dev(logits, torch.float32, "logits")
+        _dev(x, torch.float16, "x")
+        c13, b13, g13 = (t.data_ptr() for t in self.w13)
+        c2, b2, g2 = (t.data_ptr() for t in self.w2)
+
+        def call(fn, name, args):
+            def run():
+                status = fn(*args)
+                if status != MOE_OK:
+                    _check(name, status)
+            return run
+        ra = call(lib.moe_topk_route_align, "moe_topk_route_align",
+                  (logits.data_ptr(), T, E, k, self.topk_ids.data_ptr(), self.topk_w.data_ptr(),
+                   offs, sp, act, na, ws, wsb, st))
+        gu = call(lib.moe_nvfp4_gate_up_silu, "moe_nvfp4_gate_up_silu",
+                  (x.data_ptr(), c13, b13, g13, offs, sp, act, na, T, E, k, H, I, self.h.data_ptr(),
+                   ws, wsb, st))
+        dn = call(lib.moe_nvfp4_down_combine, "moe_nvfp4_down_combine",
+                  (self.h.data_ptr(), c2, b2, g2, offs, sp, act, na, self.topk_w.data_ptr(),
+                   T, E, k, H, I, self.out.data_ptr(), ws, wsb, st))
+        self.layer_call = call(lib.moe_nvfp4_moe_layer, "moe_nvfp4_moe_layer",
+                               (logits.data_ptr(), x.data_ptr(), c13, b13, g13, c2, b2, g2, T, E, k, H, I,
+                                self.topk_ids.data_ptr(), self.topk_w.data_ptr(), self.out.data_ptr(),
+                                ws, wsb, st))
+        return ra, gu, dn

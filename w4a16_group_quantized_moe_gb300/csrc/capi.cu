@@ -48,6 +48,24 @@ cudaError_t launch_decode_layer(const float *, const __half *, const uint32_t *,
                                 float *, uint32_t *, uint32_t *, uint32_t *, uint32_t *, int, size_t,
                                 cudaStream_t);
 
+cudaError_t launch_gate_up_decode_nvfp4(const __half *, const uint32_t *, const uint8_t *, const float *,
+                                        const int32_t *, const int32_t *, const int32_t *, const int32_t *, int,
+                                        int, int, int, int, __half *, uint32_t *, int, size_t, cudaStream_t);
+cudaError_t launch_down_decode_nvfp4(const __half *, const uint32_t *, const uint8_t *, const float *,
+                                     const int32_t *, const int32_t *, const int32_t *, const int32_t *,
+                                     const float *, int, int, int, int, int, __half *, float *, uint32_t *,
+                                     uint32_t *, int, size_t, cudaStream_t);
+cudaError_t launch_gate_up_tc_nvfp4(const __half *, const uint32_t *, const uint8_t *, const float *,
+                                    const int32_t *, const int32_t *, const int32_t *, const int32_t *, int, int,
+                                    int, int, int, __half *, __half *, uint32_t *, int, size_t, cudaStream_t);
+cudaError_t launch_down_tc_nvfp4(const __half *, const uint32_t *, const uint8_t *, const float *,
+                                 const int32_t *, const int32_t *, const int32_t *, const int32_t *, const float *,
+                                 int, int, int, int, int, __half *, float *, uint32_t *, int, size_t, cudaStream_t);
+cudaError_t launch_decode_layer_nvfp4(const float *, const __half *, const uint32_t *, const uint8_t *,
+                                      const float *, const uint32_t *, const uint8_t *, const float *, int, int,
+                                      int, int, int, int32_t *, float *, __half *, __half *, float *, uint32_t *,
+                                      uint32_t *, uint32_t *, uint32_t *, int, size_t, cudaStream_t);
+
 namespace {
 
 constexpr int kMaxE = 1024;
@@ -391,4 +409,115 @@ MOE_EXPORT int moe_w4a16_moe_layer(const float *logits, const uint16_t *x, const
         return st;
     return moe_w4a16_down_combine(h, w2_q, w2_s, w2_z, group_size, offsets, sorted, active, num_active,
                                   topk_w, T, E, k, H, I, out, workspace, ws_bytes, stream);
+}
+
+
+// ---------------------------------------------------------------- NVFP4 weights
+MOE_EXPORT int moe_nvfp4_gate_up_silu(const uint16_t *x, const uint32_t *w13_codes, const uint8_t *w13_bscale,
+                                      const float *w13_gscale, const int32_t *expert_offsets,
+                                      const int32_t *sorted_pair, const int32_t *active_experts,
+                                      const int32_t *num_active, int T, int E, int k, int H, int I, uint16_t *h,
+                                      void *workspace, size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(x, w13_codes, w13_bscale, w13_gscale, expert_offsets, sorted_pair, active_experts,
+                     num_active, h))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t *err = static_cast<uint32_t *>(workspace) + kCtrlErrorWord;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_gate_up_decode_nvfp4(
+            reinterpret_cast<const __half *>(x), w13_codes, w13_bscale, w13_gscale, expert_offsets, sorted_pair,
+            active_experts, num_active, T, E, k, H, I, reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, s));
+    if (tc_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_gate_up_tc_nvfp4(
+            reinterpret_cast<const __half *>(x), w13_codes, w13_bscale, w13_gscale, expert_offsets, sorted_pair,
+            active_experts, num_active, T, E, k, H, I, reinterpret_cast<__half *>(h),
+            reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + workspace_layout(T, k, H).y), err,
+            di.sms, di.smem_optin, s));
+    return MOE_ERR_UNSUPPORTED;  // the staged stream kernels read W4A16 weights only
+}
+
+MOE_EXPORT int moe_nvfp4_down_combine(const uint16_t *h, const uint32_t *w2_codes, const uint8_t *w2_bscale,
+                                      const float *w2_gscale, const int32_t *expert_offsets,
+                                      const int32_t *sorted_pair, const int32_t *active_experts,
+                                      const int32_t *num_active, const float *topk_w, int T, int E, int k, int H,
+                                      int I, uint16_t *out, void *workspace, size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(h, w2_codes, w2_bscale, w2_gscale, expert_offsets, sorted_pair, active_experts, num_active,
+                     topk_w, out))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    const WorkspaceLayout L = workspace_layout(T, k, H);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_down_decode_nvfp4(
+            reinterpret_cast<const __half *>(h), w2_codes, w2_bscale, w2_gscale, expert_offsets, sorted_pair,
+            active_experts, num_active, topk_w, T, E, k, H, I, reinterpret_cast<__half *>(out),
+            reinterpret_cast<float *>(ws + L.y), reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms,
+            di.smem_optin, s));
+    if (tc_supported(T, E, k, H, I, di.smem_optin))
+        return cuda_status(launch_down_tc_nvfp4(
+            reinterpret_cast<const __half *>(h), w2_codes, w2_bscale, w2_gscale, expert_offsets, sorted_pair,
+            active_experts, num_active, topk_w, T, E, k, H, I, reinterpret_cast<__half *>(out),
+            reinterpret_cast<float *>(ws + L.y), err, di.sms, di.smem_optin, s));
+    return MOE_ERR_UNSUPPORTED;
+}
+
+MOE_EXPORT int moe_nvfp4_moe_layer(const float *logits, const uint16_t *x, const uint32_t *w13_codes,
+                                   const uint8_t *w13_bscale, const float *w13_gscale, const uint32_t *w2_codes,
+                                   const uint8_t *w2_bscale, const float *w2_gscale, int T, int E, int k, int H,
+                                   int I, int32_t *topk_ids, float *topk_w, uint16_t *out, void *workspace,
+                                   size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(w13_codes, w13_bscale, w13_gscale, w2_codes, w2_bscale, w2_gscale)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !all_aligned(logits, x, topk_ids, topk_w, out)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) || ws_bytes < moe_layer_workspace_bytes(T, E, k, H, I))
+        return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const WorkspaceLayout W = workspace_layout(T, k, H);
+    const LayerWorkspace L = layer_workspace(T, E, k, H, I);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
+    if (layer_fusable(T, E, k, H, I, di.sms, di.smem_optin))
+        return cuda_status(launch_decode_layer_nvfp4(
+            logits, reinterpret_cast<const __half *>(x), w13_codes, w13_bscale, w13_gscale, w2_codes, w2_bscale,
+            w2_gscale, T, E, k, H, I, topk_ids, topk_w, reinterpret_cast<__half *>(out),
+            reinterpret_cast<__half *>(ws + L.h), reinterpret_cast<float *>(ws + W.y),
+            reinterpret_cast<uint32_t *>(ws + W.counters), reinterpret_cast<uint32_t *>(ws + L.done),
+            reinterpret_cast<uint32_t *>(ws + L.exitctr), err, di.sms, di.smem_optin, s));
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *sorted = reinterpret_cast<int32_t *>(ws + L.sorted);
+    int32_t *active = reinterpret_cast<int32_t *>(ws + L.active);
+    int32_t *num_active = reinterpret_cast<int32_t *>(ws + L.num_active);
+    uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
+    if (!decode_supported(T, E, k, H, I, di.smem_optin) && !tc_supported(T, E, k, H, I, di.smem_optin))
+        return MOE_ERR_UNSUPPORTED;  // checked before anything is launched
+    if ((st = moe_topk_route_align(logits, T, E, k, topk_ids, topk_w, offsets, sorted, active, num_active,
+                                   workspace, ws_bytes, stream)) != MOE_OK)
+        return st;
+    if ((st = moe_nvfp4_gate_up_silu(x, w13_codes, w13_bscale, w13_gscale, offsets, sorted, active, num_active, T,
+                                     E, k, H, I, h, workspace, ws_bytes, stream)) != MOE_OK)
+        return st;
+    return moe_nvfp4_down_combine(h, w2_codes, w2_bscale, w2_gscale, offsets, sorted, active, num_active, topk_w,
+                                  T, E, k, H, I, out, workspace, ws_bytes, stream);
 }

@@ -3,9 +3,46 @@
 // (decode_layer.cu): the per-warp task buffer and the bulk-copy ranges of a
 // task, the activation cache layout, and the dequantise-and-accumulate loop.
 #pragma once
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace moe {
+
+// Weight formats of the expert matrices:
+//   kFmtW4A16: AWQ-style uint4 codes, uint4 zero points and fp16 scales per
+//              32 elements along K; w = (q - z) * s
+//   kFmtNvfp4: E2M1 codes, an FP8 E4M3 scale per 16 elements along K (the
+//              two scales of a 32-element group sit where the fp16 group
+//              scale sits in the W4A16 layout: the same bytes per row) and
+//              an fp32 scale per expert matrix (passed where the W4A16 zero
+//              words are); w = e2m1(q) * e4m3(s) * scale[e]
+enum { kFmtW4A16 = 0, kFmtNvfp4 = 1 };
+
+// The eight E2M1 codes of one 32-bit word (code j in bits 4j..4j+3) as four
+// fp16 pairs in dequant_word's pairing: d[0] = (c0, c4), d[1] = (c1, c5),
+// d[2] = (c2, c6), d[3] = (c3, c7).  Each pair is gathered into one byte
+// (low nibble first) and converted by the CUDA fp4 intrinsic.
+__device__ __forceinline__ void e2m1_word(uint32_t w, __half2 *d) {
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;  // c0 c2 c4 c6 / c1 c3 c5 c7
+    const uint32_t L = lo | (lo >> 12), Hh = hi | (hi >> 12);            // bytes (c0 c4) (c2 c6), (c1 c5) (c3 c7)
+    const __half2_raw r0 = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(L & 0xFFu), __NV_E2M1);
+    const __half2_raw r1 = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(Hh & 0xFFu), __NV_E2M1);
+    const __half2_raw r2 = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((L >> 8) & 0xFFu), __NV_E2M1);
+    const __half2_raw r3 = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((Hh >> 8) & 0xFFu), __NV_E2M1);
+    d[0] = __half2(r0);
+    d[1] = __half2(r1);
+    d[2] = __half2(r2);
+    d[3] = __half2(r3);
+}
+
+// The two E4M3 scales of a 32-element group (the low byte covers its first
+// 16 elements) as floats.
+__device__ __forceinline__ float2 e4m3_pair(uint16_t v) {
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+    return __half22float2(__half2(r));
+}
 
 constexpr int kDecPass = 4;   // activation rows per compute pass
 constexpr int kGPI = 2;       // groups per lane worked on together
@@ -103,15 +140,17 @@ struct Cursor {
 // (s_tok[r], when given, holds that token for sorted row r);
 // step 4 reads sorted row r from cache slot r - slot_base or, when vin is
 // given, straight from vin[r][K] in global memory.
-template <int MODE, int L, int RU, int GT, int NT>
+template <int MODE, int L, int RU, int GT, int NT, int FMT = kFmtW4A16>
 __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &wg,
                                             float (&acc)[RU][DecTraits<MODE, L, RU>::nmat][kDecPass],
                                             const Cursor &c, const int *s_pairs, const uint8_t *xcb,
                                             int slot_base, const __half *vin, const TaskDims &a,
-                                            int lane, const int *s_tok = nullptr) {
+                                            int lane, const int *s_tok = nullptr, float gsc = 1.f) {
     using Tr = DecTraits<MODE, L, RU>;
     constexpr int nmat = Tr::nmat;
-    constexpr int CH = NT == 1 ? 4 : (NT == 2 ? 2 : 1);  // independent chains per product sum
+    // independent chains per product sum; with NVFP4 the two chains are the
+    // group's two 16-element blocks, each with its own scale
+    constexpr int CH = FMT == kFmtNvfp4 ? 2 : (NT == 1 ? 4 : (NT == 2 ? 2 : 1));
     const int G = GT ? GT : a.K / 32;
     const int K = 32 * G;
     const int GL = (G + L - 1) / L;  // groups per lane (compile time when GT != 0)
@@ -162,7 +201,7 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
 #pragma unroll
         for (int m0 = 0; m0 < GL; m0 += kGPI) {
             uint4 w[nmat][kGPI];
-            float sc[nmat][kGPI];
+            float sc[nmat][kGPI], sc2[nmat][kGPI];  // NVFP4: the scales of the two blocks
             ZeroPoint zq[nmat][kGPI];
             bool gok[kGPI];
 #pragma unroll
@@ -174,14 +213,20 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
                 for (int b = 0; b < nmat; ++b) {
                     if (gok[i]) {
                         w[b][i] = *reinterpret_cast<const uint4 *>(qp[b] + L * 16 * m);
-                        sc[b][i] = __half2float(*reinterpret_cast<const __half *>(sp[b] + L * 2 * m));
-                        zq[b][i] = make_zero_point(
-                            (*reinterpret_cast<const uint32_t *>(zp[b] + L * 4 * m) >> zsh[b]) & 0xFu);
+                        if (FMT == kFmtNvfp4) {
+                            const float2 s2 = e4m3_pair(*reinterpret_cast<const uint16_t *>(sp[b] + L * 2 * m));
+                            sc[b][i] = s2.x * gsc;
+                            sc2[b][i] = s2.y * gsc;
+                        } else {
+                            sc[b][i] = __half2float(*reinterpret_cast<const __half *>(sp[b] + L * 2 * m));
+                            zq[b][i] = make_zero_point(
+                                (*reinterpret_cast<const uint32_t *>(zp[b] + L * 4 * m) >> zsh[b]) & 0xFu);
+                        }
                     } else {
                         // groups past G: zero codes, zero point 0, scale 0
                         w[b][i] = make_uint4(0, 0, 0, 0);
-                        sc[b][i] = 0.f;
-                        zq[b][i] = make_zero_point(0u);
+                        sc[b][i] = sc2[b][i] = 0.f;
+                        if (FMT != kFmtNvfp4) zq[b][i] = make_zero_point(0u);
                     }
                 }
             }
@@ -201,7 +246,12 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
                     const int m = m0 + i;
                     __half2 dq[nmat][4];
 #pragma unroll
-                    for (int b = 0; b < nmat; ++b) dequant_word(dec_word(w[b][i], wd), zq[b][i], dq[b]);
+                    for (int b = 0; b < nmat; ++b) {
+                        if (FMT == kFmtNvfp4)
+                            e2m1_word(dec_word(w[b][i], wd), dq[b]);
+                        else
+                            dequant_word(dec_word(w[b][i], wd), zq[b][i], dq[b]);
+                    }
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         // activations of groups past G read as zero so sums stay finite
@@ -217,7 +267,7 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
                         }
 #pragma unroll
                         for (int b = 0; b < nmat; ++b) {
-                            __half2 &h = hs[i][b][t][wd % CH];
+                            __half2 &h = hs[i][b][t][FMT == kFmtNvfp4 ? wd / 2 : wd % CH];
                             h = __hfma2(dq[b][0], u32_as_half2(X.x), h);
                             h = __hfma2(dq[b][1], u32_as_half2(X.y), h);
                             h = __hfma2(dq[b][2], u32_as_half2(X.z), h);
@@ -232,11 +282,16 @@ __device__ __forceinline__ void dec_compute(const uint8_t *wb, const WarpGeom &w
                 for (int b = 0; b < nmat; ++b)
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        __half2 s2 = hs[i][b][t][0];
+                        if (FMT == kFmtNvfp4) {
+                            const float2 f0 = __half22float2(hs[i][b][t][0]), f1 = __half22float2(hs[i][b][t][1]);
+                            acc[ru][b][t] = fmaf(sc[b][i], f0.x + f0.y, fmaf(sc2[b][i], f1.x + f1.y, acc[ru][b][t]));
+                        } else {
+                            __half2 s2 = hs[i][b][t][0];
 #pragma unroll
-                        for (int ch = 1; ch < CH; ++ch) s2 = __hadd2(s2, hs[i][b][t][ch]);
-                        const float2 f = __half22float2(s2);
-                        acc[ru][b][t] = fmaf(sc[b][i], f.x + f.y, acc[ru][b][t]);
+                            for (int ch = 1; ch < CH; ++ch) s2 = __hadd2(s2, hs[i][b][t][ch]);
+                            const float2 f = __half22float2(s2);
+                            acc[ru][b][t] = fmaf(sc[b][i], f.x + f.y, acc[ru][b][t]);
+                        }
                     }
         }
     }

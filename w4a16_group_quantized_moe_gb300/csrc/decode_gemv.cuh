@@ -1,4 +1,4 @@
-// decode_gemv.cu -- steps 3 and 4 for decode batches (T <= 16, as far as the
+// decode_gemv.cuh -- steps 3 and 4 for decode batches (T <= 16, as far as the
 // shared-memory layout allows): the
 // latency-first weight stream.
 //
@@ -34,6 +34,7 @@
 //    CTA publishes its counts (one fence, parallel atomics); whichever CTA
 //    completes a block sums the block's k terms per token in order and writes
 //    fp16 (deterministic, no extra launch).
+#pragma once
 #include "decode_common.cuh"
 
 namespace moe {
@@ -133,7 +134,7 @@ __device__ __forceinline__ void dec_finish(float (&acc)[RU][DecTraits<MODE, L, R
             for (int t = 0; t < kDecPass; ++t) acc[ru][b][t] = 0.f;
 }
 
-template <int MODE, int L, int RU, int GT>
+template <int MODE, int L, int RU, int GT, int FMT>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs a) {
     using Tr = DecTraits<MODE, L, RU>;
     constexpr int nmat = Tr::nmat;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
 #pragma unroll
         for (int b = 0; b < nmat; ++b) {
             cp[b] = warp_copy(c.e, c.unit0 + b * a.rows, c.cnt, a.N, K);
-            tx += cp[b].q_len + cp[b].s_len + cp[b].z_len;
+            tx += cp[b].q_len + cp[b].s_len + (FMT == kFmtNvfp4 ? 0u : cp[b].z_len);
         }
         mbar_arrive_expect_tx(bar, tx);
 #pragma unroll
@@ -229,8 +230,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
             bulk_g2s(wb + b * wg.q_bytes, reinterpret_cast<const uint8_t *>(a.q) + cp[b].q_off, cp[b].q_len, bar);
             bulk_g2s(wb + nmat * wg.q_bytes + b * wg.s_bytes, reinterpret_cast<const uint8_t *>(a.s) + cp[b].s_a,
                      cp[b].s_len, bar);
-            bulk_g2s(wb + nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes,
-                     reinterpret_cast<const uint8_t *>(a.z) + cp[b].z_a, cp[b].z_len, bar);
+            if (FMT != kFmtNvfp4)  // NVFP4: no zero words (a.z holds the per-expert scales)
+                bulk_g2s(wb + nmat * (wg.q_bytes + wg.s_bytes) + b * wg.z_bytes,
+                         reinterpret_cast<const uint8_t *>(a.z) + cp[b].z_a, cp[b].z_len, bar);
         }
     };
 
@@ -258,24 +260,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
             break;
         }
         phase ^= 1u;
+        const float gsc = FMT == kFmtNvfp4 ? __ldg(reinterpret_cast<const float *>(a.z) + cur.e) : 1.f;
         // segments longer than a pass (several tokens on one expert) take more passes
         for (cur.tb = 0; cur.tb < cur.ne; cur.tb += kDecPass) {
             const int nt = min(kDecPass, cur.ne - cur.tb);
             switch (nt) {
                 case 1:
-                    dec_compute<MODE, L, RU, GT, 1>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane);
+                    dec_compute<MODE, L, RU, GT, 1, FMT>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane,
+                                                         nullptr, gsc);
                     dec_finish<MODE, L, RU, 1>(acc, cur, s_pairs, a, lane);
                     break;
                 case 2:
-                    dec_compute<MODE, L, RU, GT, 2>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane);
+                    dec_compute<MODE, L, RU, GT, 2, FMT>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane,
+                                                         nullptr, gsc);
                     dec_finish<MODE, L, RU, 2>(acc, cur, s_pairs, a, lane);
                     break;
                 case 3:
-                    dec_compute<MODE, L, RU, GT, 3>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane);
+                    dec_compute<MODE, L, RU, GT, 3, FMT>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane,
+                                                         nullptr, gsc);
                     dec_finish<MODE, L, RU, 3>(acc, cur, s_pairs, a, lane);
                     break;
                 default:
-                    dec_compute<MODE, L, RU, GT, 4>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane);
+                    dec_compute<MODE, L, RU, GT, 4, FMT>(wb, wg, acc, cur, s_pairs, xcb, 0, hc ? nullptr : a.vin, td, lane,
+                                                         nullptr, gsc);
                     dec_finish<MODE, L, RU, 4>(acc, cur, s_pairs, a, lane);
                     break;
             }
@@ -332,36 +339,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
 }
 
 // ---------------------------------------------------------------- launchers
-template <int MODE, int L, int RU, int GT>
-static cudaError_t launch_decode_t(DecodeArgs a, int num_sms, size_t smem_limit, cudaStream_t stream) {
+template <int MODE, int L, int RU, int GT, int FMT>
+inline cudaError_t launch_decode_t(DecodeArgs a, int num_sms, size_t smem_limit, cudaStream_t stream) {
     using Tr = DecTraits<MODE, L, RU>;
     a.wbytes = warp_geom(Tr::RT, Tr::nmat, a.K).bytes;
     const size_t smem = dec_layout(a.E, a.P, a.nblk, a.slots, a.K, a.wbytes).total;
     if (smem > smem_limit) return cudaErrorInvalidConfiguration;
     static int configured[128];
-    cudaError_t e = ensure_smem(decode_kernel<MODE, L, RU, GT>, configured, smem);
+    cudaError_t e = ensure_smem(decode_kernel<MODE, L, RU, GT, FMT>, configured, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_kernel<MODE, L, RU, GT>, num_sms, kDecThreads, smem, stream, a);
+    return launch_pdl(decode_kernel<MODE, L, RU, GT, FMT>, num_sms, kDecThreads, smem, stream, a);
 }
 
 // Lanes per row unit: a power of two giving each lane about five groups.
-static int lanes_for(int G) { return G >= 40 ? 8 : (G >= 20 ? 4 : (G >= 10 ? 2 : 1)); }
+inline int lanes_for(int G) { return G >= 40 ? 8 : (G >= 20 ? 4 : (G >= 10 ? 2 : 1)); }
 
 // Per-warp buffer of the decode kernels (step 3: a task of 32/L row pairs;
 // step 4: a task of 2*32/L rows).
-static uint32_t decode_wbytes(int H, int I, bool gate_up) {
+inline uint32_t decode_wbytes(int H, int I, bool gate_up) {
     const int G = (gate_up ? H : I) / 32, L = lanes_for(G);
     return gate_up ? warp_geom(32 / L, 2, H).bytes : warp_geom(2 * (32 / L), 1, I).bytes;
 }
 
 // step 4 caches every h row when they fit next to its task buffers
-static int down_slots(int T, int E, int k, int H, int I, size_t smem_limit) {
+inline int down_slots(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int P = T * k;
     const uint32_t wb = decode_wbytes(H, I, false);
     return dec_layout(E, P, H / 8, P, I, wb).total <= smem_limit ? P : 0;
 }
 
-bool decode_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
+inline bool decode_supported_impl(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int P = T * k;
     return T >= 1 && T <= kDecMaxT &&
            dec_layout(E, P, 0, T, H, decode_wbytes(H, I, true)).total <= smem_limit &&
@@ -369,7 +376,8 @@ bool decode_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
                       decode_wbytes(H, I, false)).total <= smem_limit;
 }
 
-cudaError_t launch_gate_up_decode(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
+template <int FMT>
+cudaError_t launch_gate_up_decode_f(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
                                   const int32_t *offsets, const int32_t *sorted_pair,
                                   const int32_t *active, const int32_t *num_active, int T, int E, int k,
                                   int H, int I, __half *h, uint32_t *err, int num_sms, size_t smem_limit,
@@ -383,16 +391,17 @@ cudaError_t launch_gate_up_decode(const __half *x, const uint32_t *q, const __ha
     a.slots = T;
     a.nblk = 0;
     const int G = H / 32;
-    if (G == 80) return launch_decode_t<kDecGateUp, 8, 1, 80>(a, num_sms, smem_limit, stream);
+    if (G == 80) return launch_decode_t<kDecGateUp, 8, 1, 80, FMT>(a, num_sms, smem_limit, stream);
     switch (lanes_for(G)) {
-        case 8: return launch_decode_t<kDecGateUp, 8, 1, 0>(a, num_sms, smem_limit, stream);
-        case 4: return launch_decode_t<kDecGateUp, 4, 1, 0>(a, num_sms, smem_limit, stream);
-        case 2: return launch_decode_t<kDecGateUp, 2, 1, 0>(a, num_sms, smem_limit, stream);
-        default: return launch_decode_t<kDecGateUp, 1, 1, 0>(a, num_sms, smem_limit, stream);
+        case 8: return launch_decode_t<kDecGateUp, 8, 1, 0, FMT>(a, num_sms, smem_limit, stream);
+        case 4: return launch_decode_t<kDecGateUp, 4, 1, 0, FMT>(a, num_sms, smem_limit, stream);
+        case 2: return launch_decode_t<kDecGateUp, 2, 1, 0, FMT>(a, num_sms, smem_limit, stream);
+        default: return launch_decode_t<kDecGateUp, 1, 1, 0, FMT>(a, num_sms, smem_limit, stream);
     }
 }
 
-cudaError_t launch_down_decode(const __half *h, const uint32_t *q, const __half *s, const uint32_t *z,
+template <int FMT>
+cudaError_t launch_down_decode_f(const __half *h, const uint32_t *q, const __half *s, const uint32_t *z,
                                const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
                                const int32_t *num_active, const float *topk_w, int T, int E, int k, int H,
                                int I, __half *out, float *y, uint32_t *counters, uint32_t *err,
@@ -406,13 +415,13 @@ cudaError_t launch_down_decode(const __half *h, const uint32_t *q, const __half 
     a.slots = down_slots(T, E, k, H, I, smem_limit);
     a.nblk = H / 8;
     const int G = I / 32;
-    if (G == 20) return launch_decode_t<kDecDown, 4, 2, 20>(a, num_sms, smem_limit, stream);
-    if (G == 5) return launch_decode_t<kDecDown, 1, 2, 5>(a, num_sms, smem_limit, stream);
+    if (G == 20) return launch_decode_t<kDecDown, 4, 2, 20, FMT>(a, num_sms, smem_limit, stream);
+    if (G == 5) return launch_decode_t<kDecDown, 1, 2, 5, FMT>(a, num_sms, smem_limit, stream);
     switch (lanes_for(G)) {
-        case 8: return launch_decode_t<kDecDown, 8, 2, 0>(a, num_sms, smem_limit, stream);
-        case 4: return launch_decode_t<kDecDown, 4, 2, 0>(a, num_sms, smem_limit, stream);
-        case 2: return launch_decode_t<kDecDown, 2, 2, 0>(a, num_sms, smem_limit, stream);
-        default: return launch_decode_t<kDecDown, 1, 2, 0>(a, num_sms, smem_limit, stream);
+        case 8: return launch_decode_t<kDecDown, 8, 2, 0, FMT>(a, num_sms, smem_limit, stream);
+        case 4: return launch_decode_t<kDecDown, 4, 2, 0, FMT>(a, num_sms, smem_limit, stream);
+        case 2: return launch_decode_t<kDecDown, 2, 2, 0, FMT>(a, num_sms, smem_limit, stream);
+        default: return launch_decode_t<kDecDown, 1, 2, 0, FMT>(a, num_sms, smem_limit, stream);
     }
 }
 

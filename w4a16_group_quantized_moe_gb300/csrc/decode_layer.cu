@@ -49,12 +49,13 @@ bool layer_fusable(int T, int E, int k, int H, int I, int num_sms, size_t smem_l
     return layer_plan(T, E, k, H, I, num_sms, smem_limit).ok;
 }
 
-cudaError_t launch_decode_layer(const float *logits, const __half *x, const uint32_t *q13, const __half *s13,
-                                const uint32_t *z13, const uint32_t *q2, const __half *s2,
-                                const uint32_t *z2, int T, int E, int k, int H, int I, int32_t *topk_ids,
-                                float *topk_w, __half *out, __half *h, float *y, uint32_t *blkctr,
-                                uint32_t *done, uint32_t *exitctr, uint32_t *err, int num_sms,
-                                size_t smem_limit, cudaStream_t stream) {
+template <int FMT>
+static cudaError_t launch_decode_layer_f(const float *logits, const __half *x, const uint32_t *q13,
+                                         const __half *s13, const uint32_t *z13, const uint32_t *q2,
+                                         const __half *s2, const uint32_t *z2, int T, int E, int k, int H, int I,
+                                         int32_t *topk_ids, float *topk_w, __half *out, __half *h, float *y,
+                                         uint32_t *blkctr, uint32_t *done, uint32_t *exitctr, uint32_t *err,
+                                         int num_sms, size_t smem_limit, cudaStream_t stream) {
     const LayerPlan pl = layer_plan(T, E, k, H, I, num_sms, smem_limit);
     if (!pl.ok) return cudaErrorInvalidConfiguration;
     LayerArgs a{};
@@ -67,17 +68,42 @@ cudaError_t launch_decode_layer(const float *logits, const __half *x, const uint
     const int G1 = H / 32, G2 = I / 32;
     // the geometries the layer is specified on get compile-time group counts
     if (G1 == 80 && pl.L1 == 16 && G2 == 20 && pl.L2 == 4)
-        return launch_layer_t<16, 80, 4, 20>(a, pl, num_sms, stream);
+        return launch_layer_t<16, 80, 4, 20, FMT>(a, pl, num_sms, stream);
     if (G1 == 80 && pl.L1 == 16 && G2 == 5 && pl.L2 == 1)
-        return launch_layer_t<16, 80, 1, 5>(a, pl, num_sms, stream);
+        return launch_layer_t<16, 80, 1, 5, FMT>(a, pl, num_sms, stream);
     switch (pl.L1 * 8 + pl.L2) {
-        case 16 * 8 + 4: return launch_layer_t<16, 0, 4, 0>(a, pl, num_sms, stream);
-        case 16 * 8 + 1: return launch_layer_t<16, 0, 1, 0>(a, pl, num_sms, stream);
-        case 4 * 8 + 4: return launch_layer_t<4, 0, 4, 0>(a, pl, num_sms, stream);
-        case 4 * 8 + 1: return launch_layer_t<4, 0, 1, 0>(a, pl, num_sms, stream);
-        case 1 * 8 + 4: return launch_layer_t<1, 0, 4, 0>(a, pl, num_sms, stream);
-        default: return launch_layer_t<1, 0, 1, 0>(a, pl, num_sms, stream);
+        case 16 * 8 + 4: return launch_layer_t<16, 0, 4, 0, FMT>(a, pl, num_sms, stream);
+        case 16 * 8 + 1: return launch_layer_t<16, 0, 1, 0, FMT>(a, pl, num_sms, stream);
+        case 4 * 8 + 4: return launch_layer_t<4, 0, 4, 0, FMT>(a, pl, num_sms, stream);
+        case 4 * 8 + 1: return launch_layer_t<4, 0, 1, 0, FMT>(a, pl, num_sms, stream);
+        case 1 * 8 + 4: return launch_layer_t<1, 0, 4, 0, FMT>(a, pl, num_sms, stream);
+        default: return launch_layer_t<1, 0, 1, 0, FMT>(a, pl, num_sms, stream);
     }
+}
+
+cudaError_t launch_decode_layer(const float *logits, const __half *x, const uint32_t *q13, const __half *s13,
+                                const uint32_t *z13, const uint32_t *q2, const __half *s2,
+                                const uint32_t *z2, int T, int E, int k, int H, int I, int32_t *topk_ids,
+                                float *topk_w, __half *out, __half *h, float *y, uint32_t *blkctr,
+                                uint32_t *done, uint32_t *exitctr, uint32_t *err, int num_sms,
+                                size_t smem_limit, cudaStream_t stream) {
+    return launch_decode_layer_f<kFmtW4A16>(logits, x, q13, s13, z13, q2, s2, z2, T, E, k, H, I, topk_ids, topk_w,
+                                            out, h, y, blkctr, done, exitctr, err, num_sms, smem_limit, stream);
+}
+
+// NVFP4 weights: s13 / s2 hold the E4M3 scale bytes, gs13 / gs2 the
+// per-expert scales (decode_common.cuh).
+cudaError_t launch_decode_layer_nvfp4(const float *logits, const __half *x, const uint32_t *q13,
+                                      const uint8_t *s13, const float *gs13, const uint32_t *q2, const uint8_t *s2,
+                                      const float *gs2, int T, int E, int k, int H, int I, int32_t *topk_ids,
+                                      float *topk_w, __half *out, __half *h, float *y, uint32_t *blkctr,
+                                      uint32_t *done, uint32_t *exitctr, uint32_t *err, int num_sms,
+                                      size_t smem_limit, cudaStream_t stream) {
+    return launch_decode_layer_f<kFmtNvfp4>(logits, x, q13, reinterpret_cast<const __half *>(s13),
+                                            reinterpret_cast<const uint32_t *>(gs13), q2,
+                                            reinterpret_cast<const __half *>(s2),
+                                            reinterpret_cast<const uint32_t *>(gs2), T, E, k, H, I, topk_ids, topk_w,
+                                            out, h, y, blkctr, done, exitctr, err, num_sms, smem_limit, stream);
 }
 
 }  // namespace moe

@@ -206,7 +206,7 @@ __device__ __forceinline__ void share_start(long long w, int A, int tpe, const i
     }
 }
 
-template <int L1, int GT1, int L2, int GT2>
+template <int L1, int GT1, int L2, int GT2, int FMT>
 __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(const LayerArgs a) {
     using T1 = DecTraits<kDecGateUp, L1, 1>;
     using T2 = DecTraits<kDecDown, L2, 2>;
@@ -355,11 +355,13 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         const WarpGeom &wg = gate ? wg1 : wg2;
         const int b = lane % nmat, kind = lane / nmat;  // kind 0 codes, 1 scales, 2 zeros
         const WarpCopy cp = warp_copy(cu.e, cu.unit0 + b * I, cu.cnt, N, K);
-        uint32_t tx = cp.q_len + cp.s_len + cp.z_len;
+        // NVFP4: no zero words (z13 / z2 hold the per-expert scales)
+        const int nkind = FMT == kFmtNvfp4 ? 2 : 3;
+        uint32_t tx = cp.q_len + cp.s_len + (FMT == kFmtNvfp4 ? 0u : cp.z_len);
         if (gate) tx += __shfl_xor_sync(0xffffffffu, tx, 1);
         if (lane == 0) mbar_arrive_expect_tx(bar, tx);
         __syncwarp();
-        if (kind < 3) {
+        if (kind < nkind) {
             fence_proxy_async();  // this warp's earlier reads of the slot come first
             const uint8_t *src;
             uint32_t dst, len;
@@ -465,19 +467,22 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         q0 = q1;
         Cursor cu;
         make_cursor(tp, i < n1, cu);
+        const float gsc = FMT == kFmtNvfp4
+                              ? __ldg(reinterpret_cast<const float *>(i < n1 ? a.z13 : a.z2) + cu.e)
+                              : 1.f;
         if (i < n1) {
             for (cu.tb = 0; cu.tb < cu.ne;) {
                 const int nt = cu.ne - cu.tb;
                 if (nt >= 4) {
-                    dec_compute<kDecGateUp, L1, 1, GT1, 4>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok);
+                    dec_compute<kDecGateUp, L1, 1, GT1, 4, FMT>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok, gsc);
                     layer_finish_gate_up<L1, 4>(acc1, cu, a, G2, lane);
                     cu.tb += 4;
                 } else if (nt >= 2) {
-                    dec_compute<kDecGateUp, L1, 1, GT1, 2>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok);
+                    dec_compute<kDecGateUp, L1, 1, GT1, 2, FMT>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok, gsc);
                     layer_finish_gate_up<L1, 2>(acc1, cu, a, G2, lane);
                     cu.tb += 2;
                 } else {
-                    dec_compute<kDecGateUp, L1, 1, GT1, 1>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok);
+                    dec_compute<kDecGateUp, L1, 1, GT1, 1, FMT>(wb, wg1, acc1, cu, s_pairs, cache, 0, nullptr, td1, lane, s_tok, gsc);
                     layer_finish_gate_up<L1, 1>(acc1, cu, a, G2, lane);
                     cu.tb += 1;
                 }
@@ -487,15 +492,15 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             for (cu.tb = 0; cu.tb < cu.ne;) {
                 const int nt = cu.ne - cu.tb;
                 if (nt >= 4) {
-                    dec_compute<kDecDown, L2, 2, GT2, 4>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
+                    dec_compute<kDecDown, L2, 2, GT2, 4, FMT>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane, nullptr, gsc);
                     layer_finish_down<L2, 4>(acc2, cu, s_pairs, a, lane);
                     cu.tb += 4;
                 } else if (nt >= 2) {
-                    dec_compute<kDecDown, L2, 2, GT2, 2>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
+                    dec_compute<kDecDown, L2, 2, GT2, 2, FMT>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane, nullptr, gsc);
                     layer_finish_down<L2, 2>(acc2, cu, s_pairs, a, lane);
                     cu.tb += 2;
                 } else {
-                    dec_compute<kDecDown, L2, 2, GT2, 1>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane);
+                    dec_compute<kDecDown, L2, 2, GT2, 1, FMT>(wb, wg2, acc2, cu, s_pairs, cache, hrow0, nullptr, td2, lane, nullptr, gsc);
                     layer_finish_down<L2, 1>(acc2, cu, s_pairs, a, lane);
                     cu.tb += 1;
                 }
@@ -580,9 +585,9 @@ struct LayerPlan {
 };
 
 // Cooperative launch of one instantiation: one CTA per SM, all resident.
-template <int L1, int GT1, int L2, int GT2>
+template <int L1, int GT1, int L2, int GT2, int FMT>
 cudaError_t launch_layer_t(const LayerArgs &a, const LayerPlan &pl, int num_sms, cudaStream_t stream) {
-    auto kern = decode_layer_kernel<L1, GT1, L2, GT2>;
+    auto kern = decode_layer_kernel<L1, GT1, L2, GT2, FMT>;
     static int configured[128];
     cudaError_t e = ensure_smem(kern, configured, pl.smem);
     if (e != cudaSuccess) return e;
@@ -613,9 +618,11 @@ cudaError_t launch_layer_t(const LayerArgs &a, const LayerPlan &pl, int num_sms,
     X(1, 0, 4, 0)              \
     X(1, 0, 1, 0)
 
-#define MOE_LAYER_EXTERN(L1, GT1, L2, GT2)                                                         \
-    extern template cudaError_t launch_layer_t<L1, GT1, L2, GT2>(const LayerArgs &, const LayerPlan &, \
-                                                                 int, cudaStream_t);
+#define MOE_LAYER_EXTERN(L1, GT1, L2, GT2)                                                              \
+    extern template cudaError_t launch_layer_t<L1, GT1, L2, GT2, kFmtW4A16>(const LayerArgs &, const LayerPlan &, \
+                                                                            int, cudaStream_t);               \
+    extern template cudaError_t launch_layer_t<L1, GT1, L2, GT2, kFmtNvfp4>(const LayerArgs &, const LayerPlan &, \
+                                                                            int, cudaStream_t);
 MOE_LAYER_INSTANCES(MOE_LAYER_EXTERN)
 #undef MOE_LAYER_EXTERN
 

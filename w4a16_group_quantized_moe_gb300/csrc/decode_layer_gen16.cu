@@ -4,7 +4,7 @@
 
 namespace moe {
 
-template cudaError_t launch_layer_t<16, 0, 4, 0>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
-template cudaError_t launch_layer_t<16, 0, 1, 0>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
+template cudaError_t launch_layer_t<16, 0, 4, 0, kFmtW4A16>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
+template cudaError_t launch_layer_t<16, 0, 1, 0, kFmtW4A16>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
 
 }  // namespace moe

@@ -4,7 +4,7 @@
 
 namespace moe {
 
-template cudaError_t launch_layer_t<16, 80, 4, 20>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
-template cudaError_t launch_layer_t<16, 80, 1, 5>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
+template cudaError_t launch_layer_t<16, 80, 4, 20, kFmtW4A16>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
+template cudaError_t launch_layer_t<16, 80, 1, 5, kFmtW4A16>(const LayerArgs &, const LayerPlan &, int, cudaStream_t);
 
 }  // namespace moe

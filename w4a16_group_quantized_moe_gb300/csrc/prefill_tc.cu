@@ -43,6 +43,7 @@
 #include <cuda.h>
 
 #include "align.cuh"
+#include "decode_common.cuh"
 
 namespace moe {
 
@@ -270,7 +271,10 @@ __device__ __forceinline__ int tc_unit(int b, int t, int m) {
 }
 
 // ---------------------------------------------------------------- kernel
-template <int MODE>
+// FMT: kFmtW4A16 (p.s fp16 scales, p.z zero words) or kFmtNvfp4 (p.s the
+// E4M3 scale bytes, p.z the per-expert fp32 scales; the A tiles hold
+// e2m1 * e4m3 in fp16, exact, and the epilogue applies the expert's scale).
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_kernel(const TcArgs p, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap bmap) {
     using Gm = TcGeom<MODE>;
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int j = 0; j < NG; ++j) {
                     const bool ok = 2 * kb + j < glim;
                     f[2 * j] = ok ? (uint32_t)__half_as_ushort(__ldg(sp + 2 * kb + j)) : 0u;
-                    f[2 * j + 1] = ok ? __ldg(zp + 2 * kb + j) : 0u;
+                    f[2 * j + 1] = (ok && FMT != kFmtNvfp4) ? __ldg(zp + 2 * kb + j) : 0u;
                 }
             };
             fetch(0, f0);
@@ -558,11 +562,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint8_t *codes = cring + tst + coff;
                 uint8_t *At = aring + ast;
                 ZeroPoint zpt[NG];
-                __half2 sv[NG];
+                __half2 sv[NG], sv2[NG];  // NVFP4: the scales of the group's two 16-element blocks
 #pragma unroll
                 for (int j = 0; j < NG; ++j) {
-                    zpt[j] = make_zero_point((fc[2 * j + 1] >> zsh) & 0xFu);
-                    sv[j] = __half2half2(__ushort_as_half((unsigned short)(fc[2 * j] & 0xFFFFu)));
+                    if (FMT == kFmtNvfp4) {
+                        const __half2 s2 = __half2(
+                            __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(fc[2 * j] & 0xFFFFu), __NV_E4M3));
+                        sv[j] = __low2half2(s2);
+                        sv2[j] = __high2half2(s2);
+                    } else {
+                        zpt[j] = make_zero_point((fc[2 * j + 1] >> zsh) & 0xFu);
+                        sv[j] = __half2half2(__ushort_as_half((unsigned short)(fc[2 * j] & 0xFFFFu)));
+                    }
                 }
                 uint32_t cw[WPT];
                 if (WPT == 2) {
@@ -580,11 +591,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int wi = 0; wi < WPT; ++wi) {
                     const int j = wi / 4 < NG ? wi / 4 : 0;  // group of word wi
                     __half2 d[4];
-                    dequant_word(cw[wi], zpt[j], d);
+                    __half2 scl = sv[j];
+                    if (FMT == kFmtNvfp4) {
+                        e2m1_word(cw[wi], d);
+                        if (((w0 + wi) & 3) >= 2) scl = sv2[j];  // words 2-3 of a group: its second block
+                    } else {
+                        dequant_word(cw[wi], zpt[j], d);
+                    }
                     uint32_t u[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const __half2 v2 = __hmul2(d[i], sv[j]);
+                        const __half2 v2 = __hmul2(d[i], scl);
                         u[i] = *reinterpret_cast<const uint32_t *>(&v2);
                     }
                     uint4 o;
@@ -636,6 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint32_t dacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)as * (ntile * kTcM);
             const int r0 = it.lo + it.chunk * kTcMaxN;
+            const float escale = FMT == kFmtNvfp4 ? __ldg(reinterpret_cast<const float *>(p.z) + it.e) : 1.f;
             const int u0 = it.tile * kTcM;  // first output unit of the tile
             if (MODE == kTcGateUp) {
                 // lane m holds chunk row m (one token-expert pair), column n
@@ -657,7 +675,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             float o[2];
 #pragma unroll
                             for (int i = 0; i < 2; ++i) {
-                                const float gv = __uint_as_float(g[c + i]), uv = __uint_as_float(u[c + i]);
+                                const float gv = __uint_as_float(g[c + i]) * escale,
+                                            uv = __uint_as_float(u[c + i]) * escale;
                                 o[i] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                             }
                             const __half2 h2 = __floats2half2_rn(o[0], o[1]);
@@ -689,7 +708,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int v = q4 == 0 ? prs[0] : (q4 == 1 ? prs[1] : (q4 == 2 ? prs[2] : prs[3]));
                         const int pr = __shfl_sync(0xffffffffu, v, col & 31);
                         if (unit < p.rows && col < nrows && pr >= 0 && pr < p.P)
-                            p.y_out[(size_t)pr * p.rows + unit] = __uint_as_float(g[c]);
+                            p.y_out[(size_t)pr * p.rows + unit] = __uint_as_float(g[c]) * escale;
                     }
                 }
             }
@@ -761,7 +780,7 @@ cudaError_t rows_map(CUtensorMap *map, const __half *base, long long rows, int K
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, const __half *brows, long long nbrows, int num_sms,
                       size_t smem_limit, cudaStream_t stream) {
     using Gm = TcGeom<MODE>;
@@ -791,9 +810,9 @@ cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, const __half *brows, 
     e = rows_map(&bmap, brows, nbrows, a.K, kTcMaxN);
     if (e != cudaSuccess) return e;
     static int configured[128];
-    e = ensure_smem(tc_kernel<MODE>, configured, smem);
+    e = ensure_smem(tc_kernel<MODE, FMT>, configured, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(tc_kernel<MODE>, num_sms, kTcThreads, smem, stream, a, map, bmap);
+    return launch_pdl(tc_kernel<MODE, FMT>, num_sms, kTcThreads, smem, stream, a, map, bmap);
 }
 
 // xs[r] = x[token of sorted row r], each 8-element block in the
@@ -841,7 +860,8 @@ bool tc_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
                smem_limit;
 }
 
-cudaError_t launch_gate_up_tc(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
+template <int FMT>
+static cudaError_t launch_gate_up_tc_f(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
                               const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
                               const int32_t *num_active, int T, int E, int k, int H, int I, __half *h, __half *xperm,
                               uint32_t *err, int num_sms, size_t smem_limit, cudaStream_t stream) {
@@ -855,13 +875,33 @@ cudaError_t launch_gate_up_tc(const __half *x, const uint32_t *q, const __half *
     cudaError_t e = launch_pdl(sorted_rows_kernel, num_sms * 8, 256, 0, stream, reinterpret_cast<const uint4 *>(x),
                                sorted_pair, k, T * k, H / 8, reinterpret_cast<uint4 *>(xperm));
     if (e != cudaSuccess) return e;
-    return launch_tc<kTcGateUp>(a, q, xperm, (long long)T * k, num_sms, smem_limit, stream);
+    return launch_tc<kTcGateUp, FMT>(a, q, xperm, (long long)T * k, num_sms, smem_limit, stream);
+}
+
+cudaError_t launch_gate_up_tc(const __half *x, const uint32_t *q, const __half *s, const uint32_t *z,
+                              const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
+                              const int32_t *num_active, int T, int E, int k, int H, int I, __half *h, __half *xperm,
+                              uint32_t *err, int num_sms, size_t smem_limit, cudaStream_t stream) {
+    return launch_gate_up_tc_f<kFmtW4A16>(x, q, s, z, offsets, sorted_pair, active, num_active, T, E, k, H, I, h,
+                                          xperm, err, num_sms, smem_limit, stream);
+}
+
+// NVFP4 weights: s the E4M3 scale bytes, gs the per-expert scales
+cudaError_t launch_gate_up_tc_nvfp4(const __half *x, const uint32_t *q, const uint8_t *s, const float *gs,
+                                    const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
+                                    const int32_t *num_active, int T, int E, int k, int H, int I, __half *h,
+                                    __half *xperm, uint32_t *err, int num_sms, size_t smem_limit,
+                                    cudaStream_t stream) {
+    return launch_gate_up_tc_f<kFmtNvfp4>(x, q, reinterpret_cast<const __half *>(s),
+                                          reinterpret_cast<const uint32_t *>(gs), offsets, sorted_pair, active,
+                                          num_active, T, E, k, H, I, h, xperm, err, num_sms, smem_limit, stream);
 }
 
 cudaError_t launch_combine(const float *y, const float *topk_w, int T, int k, int H, __half *out,
                            cudaStream_t stream);
 
-cudaError_t launch_down_tc(const __half *h, const uint32_t *q, const __half *s, const uint32_t *z,
+template <int FMT>
+static cudaError_t launch_down_tc_f(const __half *h, const uint32_t *q, const __half *s, const uint32_t *z,
                            const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
                            const int32_t *num_active, const float *topk_w, int T, int E, int k, int H, int I,
                            __half *out, float *y, uint32_t *err, int num_sms, size_t smem_limit,
@@ -872,9 +912,28 @@ cudaError_t launch_down_tc(const __half *h, const uint32_t *q, const __half *s, 
     a.T = T; a.k = k; a.P = T * k;
     a.offsets = offsets; a.sorted_pair = sorted_pair; a.active = active; a.num_active = num_active;
     a.y_out = y; a.err = err;
-    cudaError_t e = launch_tc<kTcDown>(a, q, h, (long long)T * k, num_sms, smem_limit, stream);
+    cudaError_t e = launch_tc<kTcDown, FMT>(a, q, h, (long long)T * k, num_sms, smem_limit, stream);
     if (e != cudaSuccess) return e;
     return launch_combine(y, topk_w, T, k, H, out, stream);
+}
+
+cudaError_t launch_down_tc(const __half *h, const uint32_t *q, const __half *s, const uint32_t *z,
+                           const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
+                           const int32_t *num_active, const float *topk_w, int T, int E, int k, int H, int I,
+                           __half *out, float *y, uint32_t *err, int num_sms, size_t smem_limit,
+                           cudaStream_t stream) {
+    return launch_down_tc_f<kFmtW4A16>(h, q, s, z, offsets, sorted_pair, active, num_active, topk_w, T, E, k, H, I,
+                                       out, y, err, num_sms, smem_limit, stream);
+}
+
+cudaError_t launch_down_tc_nvfp4(const __half *h, const uint32_t *q, const uint8_t *s, const float *gs,
+                                 const int32_t *offsets, const int32_t *sorted_pair, const int32_t *active,
+                                 const int32_t *num_active, const float *topk_w, int T, int E, int k, int H, int I,
+                                 __half *out, float *y, uint32_t *err, int num_sms, size_t smem_limit,
+                                 cudaStream_t stream) {
+    return launch_down_tc_f<kFmtNvfp4>(h, q, reinterpret_cast<const __half *>(s),
+                                       reinterpret_cast<const uint32_t *>(gs), offsets, sorted_pair, active,
+                                       num_active, topk_w, T, E, k, H, I, out, y, err, num_sms, smem_limit, stream);
 }
 
 }  // namespace moe
