@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--timeline", type=int, default=0,
                     help="also run this many steps with the decode layer's phase timestamps on "
                          "and report their summary (decode batches only)")
+    ap.add_argument("--sweep-paths", default="",
+                    help="comma-separated batch sizes: instead of the bench line, time the step calls on "
+                         "every kernel family (and the one-call layer) at each T on the Qwen4Exp and TP4-shard "
+                         "geometries, one JSON line per (geometry, T)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the secondary per-workload figures")
     ap.add_argument("--layers", type=int, default=0,
@@ -90,30 +94,31 @@ def tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def layer_launches(T: int, k: int) -> int:
-    """Kernels the one-call layer launches for T tokens, following the
-    dispatch in capi.cu, decode_gemv.cu and prefill_tc.cu.
-    - Decode batches (T <= 8): one cooperative kernel.
-    - Otherwise route+align, in one launch for T <= 32, then gate/up and
-      down.
-    - On the tensor-core path (T >= 9 and T*k >= 128): gate/up adds the
-      sorted x gather and down adds the combine.
-    - On the decode step kernels (up to 16 tokens, when their shared-memory
-      layout fits; on the benchmarked geometry that happens only below 128
-      pairs): one launch per step.
-    - On the stream kernels: down adds the combine."""
+def layer_launches(moe, T: int, E: int, k: int, H: int, I: int) -> int:
+    """Kernels the one-call layer launches for a shape, following the
+    dispatch in capi.cu (moe_step_kernel_path reports the step kernels'
+    family) and the kernel files:
+    - decode batches that fit the one-launch layer (T <= 8): one cooperative
+      kernel;
+    - otherwise route+align (one launch for T <= 32, else two), then
+      - decode kernels: gate/up, down with the combine fused (2);
+      - tensor cores: x gather + gate/up, down + combine (4);
+      - stream kernels: gate/up, down (+ the combine kernel above 8 tokens)."""
     if T <= 8:
         return 1
     ra = 1 if T <= 32 else 2
-    if T * k >= 128:
-        return ra + 2 + 2
-    return ra + 1 + (1 if T <= 16 else 2)
+    path = moe.moe_step_kernel_path(T, E, k, H, I)
+    if path == moe.MOE_PATH_DECODE:
+        return ra + 2
+    if path == moe.MOE_PATH_TENSOR_CORE:
+        return ra + 4
+    return ra + 1 + (1 if T <= 8 else 2)
 
 
-def active_bytes(A: int, T: int, k: int, H: int, I: int):
+def active_bytes(A: int, T: int, k: int, H: int, I: int, fmt: str = "w4a16"):
     """Algorithmic bytes of one layer step and of the gate/up launch."""
     from w4a16_group_quantized_moe_gb300 import inputs
-    b = inputs.bytes_per_expert(H, I)
+    b = inputs.bytes_per_expert_nvfp4(H, I) if fmt == "nvfp4" else inputs.bytes_per_expert(H, I)
     P = T * k
     E_meta = 0
     gate_up = A * b["w13"] + T * H * 2 + P * I * 2
@@ -271,14 +276,14 @@ def whole_job_rate(world: int, tokens_per_step: int, steps: int, max_ms: float) 
     return world * tokens_per_step * steps / (max_ms / 1e3)
 
 
-def copies_needed(wl) -> int:
+def copies_needed(wl, fmt: str = "w4a16") -> int:
     """Distinct weight copies a workload's steps rotate over so that every
     step reads its active weights from HBM: enough that the other copies'
     active weights stream more than twice the 126 MB L2 between two uses of
     a copy (at least 4, at most 16)."""
     from w4a16_group_quantized_moe_gb300 import inputs
     sh = wl.shape
-    b = inputs.bytes_per_expert(sh.H, sh.I)
+    b = inputs.bytes_per_expert_nvfp4(sh.H, sh.I) if fmt == "nvfp4" else inputs.bytes_per_expert(sh.H, sh.I)
     per_step = min(sh.E, sh.T * sh.k) * (b["w13"] + b["w2"])
     return max(4, min(16, int(np.ceil(2 * 126e6 / max(per_step, 1))) + 1))
 
@@ -378,13 +383,14 @@ class LayerRig:
     in turn), `sets` router-logit/activation sets, bound layer calls, and
     per-step CUDA-event timing on the launching stream."""
 
-    def __init__(self, moe, wl, copies, dev, sets: int, NL: int):
+    def __init__(self, moe, wl, copies, dev, sets: int, NL: int, fmt: str = "w4a16"):
         import torch
         from w4a16_group_quantized_moe_gb300 import inputs
         sh = wl.shape
-        self.wl, self.sh, self.moe, self.dev = wl, sh, moe, dev
+        self.wl, self.sh, self.moe, self.dev, self.fmt = wl, sh, moe, dev, fmt
         self.NL = min(NL, len(copies))
-        self.layers = [moe.MoELayer(c13, c2, sh.T, sh.k, device=dev) for c13, c2 in copies[:self.NL]]
+        cls = moe.MoELayerNvfp4 if fmt == "nvfp4" else moe.MoELayer
+        self.layers = [cls(c13, c2, sh.T, sh.k, device=dev) for c13, c2 in copies[:self.NL]]
         self.sets = []
         for si in range(sets):
             lg, xx = inputs.make_activations(sh.T, sh.H, sh.E, wl.seed + 1000 + si, wl.hot_experts, wl.hot_bias)
@@ -396,10 +402,9 @@ class LayerRig:
         self.calls = [ly.layer_call for ly in self.layers]
         # active experts of every set (for the algorithmic bytes)
         self.A_of = []
-        r0, a0, _, _ = self.steps4[0]
         for lg, xx in self.sets:
             self.logits_buf.copy_(lg)
-            r0(); a0()
+            self.layers[0].route_align_call()
             self.A_of.append(int(self.layers[0].meta[3].item()))
 
     def stage(self, s):
@@ -411,8 +416,10 @@ class LayerRig:
         self.calls[s % self.NL]()
 
     def four_calls(self, s):
-        r, a_, g, d = self.steps4[s % self.NL]
-        r(); a_(); g(); d()
+        """The step calls (route, align, gate/up, down; NVFP4: route+align,
+        gate/up, down)."""
+        for f in self.steps4[s % self.NL]:
+            f()
 
     def timed(self, n, first, fn, flush=None):
         """Per-step milliseconds of fn over n steps starting at step `first`."""
@@ -443,13 +450,15 @@ class LayerRig:
         return np.array([self.A_of[(first + s) % len(self.sets)] for s in range(n)])
 
 
-def roofline_entry(wl, ms, A_steps):
-    """Roofline of one workload from per-step times: HBM bytes for decode
-    batches, tensor FLOPs otherwise (the algorithmic work)."""
+def roofline_entry(wl, ms, A_steps, fmt: str = "w4a16"):
+    """Roofline of one workload from per-step times: HBM bytes up to 128
+    tokens (each active expert sees a few rows: about 9 FLOP per weight byte
+    at 128 tokens on the Qwen4Exp geometry, far below the ridge of about
+    280), tensor FLOPs above (the algorithmic work)."""
     sh = wl.shape
     T, H, I, k = sh.T, sh.H, sh.I, sh.k
-    if T <= 8:
-        lb = np.array([active_bytes(int(a), T, k, H, I)[0] for a in A_steps])
+    if T <= 128:
+        lb = np.array([active_bytes(int(a), T, k, H, I, fmt)[0] for a in A_steps])
         gbs = float(lb.sum() / (ms.sum() / 1e3) / 1e9)
         peak, kind, _ = peaks()
         return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
@@ -462,29 +471,30 @@ def roofline_entry(wl, ms, A_steps):
             "peak_source": tsrc, "flops_per_step": flops}
 
 
-def per_config_figures(moe, dev, geoms, names, sets: int):
+def per_config_figures(moe, dev, geoms, names, sets: int, fmt: str = "w4a16"):
     """Median/mean layer time, tokens/s and roofline fraction of each named
     workload through the one-call layer (a few seconds of GPU time each)."""
     from w4a16_group_quantized_moe_gb300 import inputs
     out = []
     for name in names:
-        wl = inputs.ALL[name]
+        wl = name if isinstance(name, inputs.Workload) else inputs.ALL[name]
+        name = wl.name
         copies = geoms(wl)
         big = wl.shape.T > 8
-        rig = LayerRig(moe, wl, copies, dev, min(sets, 8), copies_needed(wl))
+        rig = LayerRig(moe, wl, copies, dev, min(sets, 8), copies_needed(wl, fmt), fmt)
         warm, steps = (3, 30) if big else (20, 400)
         rig.timed(warm, 0, rig.one_call)
         rig.check_errors(f"during warm-up of {name}")
         ms = rig.timed(steps, warm, rig.one_call)
         rig.check_errors(f"during {name}")
         A = rig.A_steps(warm, steps)
-        roof = roofline_entry(wl, ms, A)
+        roof = roofline_entry(wl, ms, A, fmt)
         out.append({"workload": name, "steps": steps, "warmup": warm,
                     "layer_us_median": float(np.median(ms) * 1e3), "layer_us_mean": float(ms.mean() * 1e3),
                     "tokens_per_s": wl.shape.T * steps / (ms.sum() / 1e3),
                     "mean_active_experts": float(A.mean()),
                     "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")},
-                    "gpu_launches_per_step": layer_launches(wl.shape.T, wl.shape.k)})
+                    "gpu_launches_per_step": layer_launches(moe, *(getattr(wl.shape, f) for f in "TEkHI"))})
         del rig
     return out
 
@@ -543,6 +553,81 @@ PER_CONFIG = ("qwen4exp_decode_T1_H2560_I640_E512_k10", "qwen4exp_decode_T2_H256
               "tp4shard_decode_T4_H2560_I160_E512_k10_hot16", "tp4shard_decode_T8_H2560_I160_E512_k10_hot16")
 
 
+# batches between decode and prefill on the Qwen4Exp geometry (one-call layer)
+MID_SIZES = (9, 12, 16, 24, 32, 64, 128)
+
+
+def mid_size_workloads():
+    from w4a16_group_quantized_moe_gb300 import inputs
+    return [inputs.Workload(f"qwen4exp_mid_T{T}_H2560_I640_E512_k10", inputs.MoEShape(T, 2560, 640, 512, 10))
+            for T in MID_SIZES]
+
+
+# the same layer with NVFP4 weights (moe_nvfp4_moe_layer)
+NVFP4_CONFIG = ("qwen4exp_decode_T1_H2560_I640_E512_k10", "qwen4exp_decode_T2_H2560_I640_E512_k10",
+                "qwen4exp_decode_T4_H2560_I640_E512_k10", "qwen4exp_decode_T8_H2560_I640_E512_k10",
+                "qwen4exp_prefill_T4096_H2560_I640_E512_k10")
+
+
+SWEEP_GEOMS = (("qwen4exp", 2560, 640, 512, 10, (), 0.0),
+               ("tp4shard", 2560, 160, 512, 10, tuple(range(16)), 2.0))
+
+
+def sweep_paths(moe, dev, ts, steps: int = 200):
+    """For each geometry and T: mean us per layer of the one-call layer, of
+    the fused route+align call, of route then align, and of the step calls
+    with every kernel family forced (None where the family cannot take the
+    shape).  Weights rotate over copies as in the bench line."""
+    import torch
+    from w4a16_group_quantized_moe_gb300 import inputs
+    rows = []
+    for gname, H, I, E, k, hot, bias in SWEEP_GEOMS:
+        w13, w2 = inputs.make_weights(E, H, I, 0)
+        base = (moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev))
+        del w13, w2
+        copies = [base]
+        for T in ts:
+            wl = inputs.Workload(f"{gname}_T{T}", inputs.MoEShape(T, H, I, E, k), hot_experts=hot, hot_bias=bias)
+            NL = copies_needed(wl)
+            while len(copies) < NL:
+                copies.append((tuple(t.clone() for t in base[0]), tuple(t.clone() for t in base[1])))
+            rig = LayerRig(moe, wl, copies, dev, 8, NL)
+            row = {"geom": gname, "T": T, "auto_path": moe.moe_step_kernel_path(T, E, k, H, I)}
+            warm = 5 if T > 64 else 20
+            rig.timed(warm, 0, rig.one_call)
+            row["one_call_us"] = float(rig.timed(steps, warm, rig.one_call).mean() * 1e3)
+
+            def ra(s):
+                rig.layers[s % rig.NL].route_align_call()
+
+            def r_then_a(s):
+                st = rig.steps4[s % rig.NL]
+                st[0]()
+                st[1]()
+            for name, fn in (("route_align_fused_us", ra), ("route_then_align_us", r_then_a)):
+                rig.timed(warm, 0, fn)
+                row[name] = float(rig.timed(steps, warm, fn).mean() * 1e3)
+            for p, pname in ((moe.MOE_PATH_DECODE, "decode"), (moe.MOE_PATH_TENSOR_CORE, "tensor_core"),
+                             (moe.MOE_PATH_STREAM, "stream")):
+                for ly in rig.layers:
+                    ly.path = p
+                try:
+                    rig.steps4 = [ly.bind(rig.logits_buf, rig.x_buf, rig.stream) for ly in rig.layers]
+                    rig.timed(warm, 0, rig.four_calls)
+                    row[pname + "_us"] = float(rig.timed(steps, warm, rig.four_calls).mean() * 1e3)
+                    rig.check_errors(f"{gname} T{T} {pname}")
+                except moe.MoEError as e:
+                    if e.status != moe.MOE_ERR_UNSUPPORTED:
+                        raise
+                    row[pname + "_us"] = None
+            print(json.dumps(row), flush=True)
+            rows.append(row)
+            del rig
+        del copies, base
+        torch.cuda.empty_cache()
+    return rows
+
+
 def main():
     args = parse()
     from w4a16_group_quantized_moe_gb300 import inputs
@@ -562,6 +647,9 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     import w4a16_group_quantized_moe_gb300 as moe
+    if args.sweep_paths:
+        sweep_paths(moe, dev, [int(t) for t in args.sweep_paths.split(",")])
+        return
 
     sh = wl.shape
     T, H, I, E, k = sh.T, sh.H, sh.I, sh.E, sh.k
@@ -570,13 +658,17 @@ def main():
     # that geometry (the copies are a stack of MoE layers used in turn)
     geo_cache = {}
 
-    def geoms(w, need=None):
-        key = (w.shape.E, w.shape.H, w.shape.I, w.seed)
-        n = max(copies_needed(w), need or 0)
+    def geoms(w, need=None, fmt="w4a16"):
+        key = (w.shape.E, w.shape.H, w.shape.I, w.seed, fmt)
+        n = max(copies_needed(w, fmt), need or 0)
         if key not in geo_cache:
             geo_cache.clear()
-            w13, w2 = inputs.make_weights(*key)
-            geo_cache[key] = [(moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev))]
+            if fmt == "nvfp4":
+                w13, w2 = inputs.make_weights_nvfp4(*key[:4])
+                geo_cache[key] = [(moe.to_device_weights_nvfp4(w13, dev), moe.to_device_weights_nvfp4(w2, dev))]
+            else:
+                w13, w2 = inputs.make_weights(*key[:4])
+                geo_cache[key] = [(moe.to_device_weights(w13, dev), moe.to_device_weights(w2, dev))]
             del w13, w2
         c = geo_cache[key]
         while len(c) < n:
@@ -634,10 +726,16 @@ def main():
             timeline = phase_timeline(moe, rig, args.timeline, dev)
         del rig
 
-        per_config = None
+        per_config = nvfp4 = mid = None
         if rank == 0 and not args.no_per_config:
             per_config = per_config_figures(moe, dev, geoms, [n for n in PER_CONFIG if n != wl.name],
                                             args.sets)
+            mid = per_config_figures(moe, dev, geoms, mid_size_workloads(), args.sets)
+            for m in mid:
+                m["path"] = {1: "decode", 2: "tensor_core", 3: "stream"}.get(
+                    moe.moe_step_kernel_path(int(m["workload"].split("_T")[1].split("_")[0]), 512, 10, 2560, 640))
+            nvfp4 = per_config_figures(moe, dev, lambda w: geoms(w, fmt="nvfp4"), NVFP4_CONFIG, args.sets,
+                                       fmt="nvfp4")
     geo_cache.clear()
 
     tot_ms = max_over_ranks(float(layer_ms.sum()), dev)
@@ -668,19 +766,21 @@ def main():
             "dtype": "f16", "data": "synthetic",
             "config": bench_config(wl, world, args.sets),
             "mean_active_experts": float(A_steps.mean()),
-            "layer_hbm_gbs": roof["achieved"] if T <= 8 else None,
+            "layer_hbm_gbs": roof["achieved"] if roof["bound"] == "hbm" else None,
             "layer_us": {"median": med(layer_ms), "p10": float(np.percentile(layer_ms, 10) * 1e3),
                          "p90": float(np.percentile(layer_ms, 90) * 1e3)},
             "layer_us_l2_flushed_each_step": med(flushed_ms),
             "layer_us_four_step_calls": med(four_ms),
             "roofline": roof,
             "per_config": per_config,
+            "nvfp4_per_config": nvfp4,
+            "mid_size": mid,
             "timeline": timeline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,
                     "d2h_bytes_per_step": T * H * 2, "steps": e2e_steps},
-            "gpu_launches": layer_launches(T, k) * args.steps,
+            "gpu_launches": layer_launches(moe, T, E, k, H, I) * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line))

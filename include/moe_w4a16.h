@@ -113,12 +113,14 @@ int moe_get_device_error(void *workspace, size_t ws_bytes, uint32_t *flag_out,
 /* Which kernels the step calls (moe_w4a16_gate_up_silu and
  * moe_w4a16_down_combine) run for a shape on the current device, chosen from
  * the shape alone (host; queries the device's SM count and shared-memory
- * limit on first use).  Returns MOE_PATH_NONE for sizes the library rejects,
- * for T == 0 and when no device is usable. */
+ * limit on first use): the per-shape table of measured choices where it
+ * lists the shape, else a rule on the shape.  Returns MOE_PATH_NONE for
+ * sizes the library rejects, for T == 0 and when no device is usable. */
 #define MOE_PATH_NONE 0
 #define MOE_PATH_DECODE 1       /* latency-first weight-streaming decode kernels */
 #define MOE_PATH_TENSOR_CORE 2  /* tcgen05 grouped contractions */
 #define MOE_PATH_STREAM 3       /* staged CUDA-core streaming kernels */
+#define MOE_PATH_AUTO 0         /* as an argument: the library's choice */
 int moe_step_kernel_path(int T, int E, int k, int H, int I);
 
 /* Step 1, router.  For each token t: softmax over logits[t][0..E), the k
@@ -256,9 +258,10 @@ int moe_w4a16_moe_layer(const float *logits, const uint16_t *x,
  * activations in fp16 within each 16-element block, scaled by the block's
  * E4M3 scale and the expert's scale in fp32 (decode kernels), or the MMA
  * operand e2m1 * e4m3 in fp16 (exact) with fp32 accumulation and the
- * expert's scale applied to the accumulator (tensor-core kernels).  Shapes
- * that neither the decode kernels nor the tensor-core kernels take (the
- * staged stream band) return MOE_ERR_UNSUPPORTED before any launch.
+ * expert's scale applied to the accumulator (tensor-core kernels): the
+ * decode kernels up to 16 tokens where their layout fits, else the tensor
+ * cores (there are no stream kernels for this format).  A shape neither
+ * takes returns MOE_ERR_UNSUPPORTED before any launch.
  * Scale products |e4m3 * gscale| and activations must keep each block's fp16
  * partial sum finite. */
 int moe_nvfp4_gate_up_silu(const uint16_t *x, const uint32_t *w13_codes, const uint8_t *w13_bscale,
@@ -279,6 +282,83 @@ int moe_nvfp4_moe_layer(const float *logits, const uint16_t *x, const uint32_t *
                         const uint8_t *w2_bscale, const float *w2_gscale, int T, int E, int k, int H,
                         int I, int32_t *topk_ids, float *topk_w, uint16_t *out, void *workspace,
                         size_t ws_bytes, void *stream);
+
+/* ---- The steps on either side of the layer.
+ *
+ * Router logits, the step ahead of moe_topk_route.  The grouped-decode work
+ * takes the router's fp32 logits as given ("[Perf][SM70] Narrow Qwen3.8 AWQ
+ * active grouped decode", section Purpose: 512 experts, top-k 10, hidden
+ * 2560); the model's gate is a bias-free linear map from the hidden state
+ * to one score per expert:
+ *     logits[t][e] = sum over h of x[t][h] * w_router[e][h]
+ *   x        f16 [T][H]   hidden states (the layer's x)
+ *   w_router f16 [E][H]   one row per expert (a linear layer's weight)
+ *   logits   f32 [T][E]   out
+ * Products of fp16 values are exact in fp32 and are summed in fp32 (order
+ * unspecified).  T <= 16: a weight-streaming GEMV; larger T: tcgen05 tensor
+ * cores.  Sizes as for moe_topk_route with k = 1 (H a multiple of 32).
+ * `workspace` is optional (NULL, or at least 256 bytes, zero-filled): it
+ * receives MOE_DEVERR_WAIT_TIMEOUT if a tensor-core wait gives up. */
+int moe_router_logits(const uint16_t *x, const uint16_t *w_router, int T, int E, int H, float *logits,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/* Router logits, steps 1 and 2 in one call: the outputs of
+ * moe_router_logits followed by moe_topk_route_align on those logits (so
+ * the routing is exactly that of moe_topk_route applied to `logits`).  For
+ * T <= 16 one launch: the last CTA of the GEMV to finish (an atomic ticket
+ * in the workspace's control block; no CTA waits for another) routes and
+ * groups.  `workspace` is required: at least 256 bytes, zero-filled before
+ * first use, left reusable after every call that completed without a
+ * device error; calls sharing it must be ordered on one stream. */
+int moe_router_route_align(const uint16_t *x, const uint16_t *w_router, int T, int E, int k, int H,
+                           float *logits, int32_t *topk_ids, float *topk_w, int32_t *expert_offsets,
+                           int32_t *sorted_pair, int32_t *active_experts, int32_t *num_active,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/* AWQ checkpoint import.  "[Model][SM70] Support Qwen3.8 Flash Next with
+ * PLE offload", section Purpose, names the AWQ g32 metadata adapter that
+ * feeds the grouped decode; the checkpoint layout is the public AWQ "GEMM"
+ * packing of a linear layer with input size K and output size N (experts
+ * stacked on a leading E axis):
+ *   awq_qweight u32 [E][K][N/8]    nibble i of word [kk][c] = code of column 8c + ORDER[i]
+ *   awq_qzeros  u32 [E][K/32][N/8] nibble i of word [g][c]  = zero of column 8c + ORDER[i]
+ *   awq_scales  f16 [E][K/32][N]
+ *   ORDER = (0, 2, 4, 6, 1, 3, 5, 7); w = (code - zero) * scale.
+ * Writes the same (code, zero, scale) of every element into rows
+ * [row0, row0 + N) of a matrix stack in this library's layout with N_dst
+ * rows per expert: qweight [E][N_dst][K/8], scales [E][N_dst][K/32],
+ * qzeros [E][N_dst/8][K/32] (e.g. a gate layer at row0 = 0 and the up
+ * layer at row0 = I of W13; a down layer at row0 = 0 of W2).  Only the
+ * destination rows named are written (their zero words whole: row0 and N
+ * are multiples of 8).  Requires K % 32 == 0, N % 8 == 0, N_dst % 8 == 0,
+ * row0 % 8 == 0, row0 + N <= N_dst, group_size == 32; E <= 1024, K <= 65536.
+ * Source and destination must not overlap.  Bit-exact (a permutation of
+ * bits); asynchronous on `stream`, no workspace. */
+int moe_awq_import(const uint32_t *awq_qweight, const uint32_t *awq_qzeros, const uint16_t *awq_scales,
+                   int E, int K, int N, int group_size, uint32_t *qweight, uint16_t *scales,
+                   uint32_t *qzeros, int N_dst, int row0, void *stream);
+
+/* Steps 3 and 4 with the kernel family named: `path` is MOE_PATH_AUTO (the
+ * choice of moe_step_kernel_path, as the calls without _ex make), or
+ * MOE_PATH_DECODE, MOE_PATH_TENSOR_CORE or MOE_PATH_STREAM to force one.
+ * Every family computes the same step (results within the layer's
+ * tolerance of each other; h is in sorted-row order on every path), so the
+ * two steps of a layer may run on different paths.  A forced path that
+ * cannot take the shape returns MOE_ERR_UNSUPPORTED before any launch; any
+ * other value is MOE_ERR_INVALID_ARG.  Other arguments and rules as for the
+ * calls without _ex. */
+int moe_w4a16_gate_up_silu_ex(const uint16_t *x, const uint32_t *w13_q, const uint16_t *w13_s,
+                              const uint32_t *w13_z, int group_size, const int32_t *expert_offsets,
+                              const int32_t *sorted_pair, const int32_t *active_experts,
+                              const int32_t *num_active, int T, int E, int k, int H, int I, uint16_t *h,
+                              void *workspace, size_t ws_bytes, int path, void *stream);
+
+int moe_w4a16_down_combine_ex(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
+                              const uint32_t *w2_z, int group_size, const int32_t *expert_offsets,
+                              const int32_t *sorted_pair, const int32_t *active_experts,
+                              const int32_t *num_active, const float *topk_w, int T, int E, int k, int H,
+                              int I, uint16_t *out, void *workspace, size_t ws_bytes, int path,
+                              void *stream);
 
 /* Step 4 for callers that cannot allocate device memory.  The paper has no
  * counterpart: this is a convenience of this library.  Some callers are not

@@ -33,12 +33,26 @@ def test_reference_arm_prints_one_json_line():
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
+class _FakeLib:
+    """moe_step_kernel_path by a fixed rule (no device here)."""
+    MOE_PATH_DECODE, MOE_PATH_TENSOR_CORE, MOE_PATH_STREAM = 1, 2, 3
+
+    def __init__(self, path):
+        self.path = path
+
+    def moe_step_kernel_path(self, T, E, k, H, I):
+        return self.path
+
+
 def test_launch_count_follows_the_dispatch():
-    assert bench.layer_launches(1, 10) == 1        # one cooperative kernel
-    assert bench.layer_launches(8, 10) == 1
-    assert bench.layer_launches(4096, 10) == 6     # route, align, gather, gate/up, down, combine
-    assert bench.layer_launches(32, 10) == 5       # route+align in one launch
-    assert bench.layer_launches(9, 10) == 3        # decode step kernels
+    dec, tc, st = _FakeLib(1), _FakeLib(2), _FakeLib(3)
+    q = (512, 10, 2560, 640)
+    assert bench.layer_launches(dec, 1, *q) == 1        # one cooperative kernel
+    assert bench.layer_launches(tc, 8, *q) == 1
+    assert bench.layer_launches(tc, 4096, *q) == 6      # route, align, gather, gate/up, down, combine
+    assert bench.layer_launches(tc, 32, *q) == 5        # route+align in one launch
+    assert bench.layer_launches(dec, 9, *q) == 3        # decode step kernels, combine fused
+    assert bench.layer_launches(st, 12, *q) == 4        # stream kernels + combine
 
 
 def _rank_main(rank, port, q):

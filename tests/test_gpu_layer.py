@@ -81,11 +81,15 @@ OTHER_CASES = [
     # last down item wholly past H
     inputs.Workload("tc_T80_H96_I96_E8_k3", inputs.MoEShape(80, 96, 96, 8, 3)),
     inputs.Workload("tc_T64_H384_I64_E16_k2", inputs.MoEShape(64, 384, 64, 16, 2)),
-    # mid-size dispatch on the full hidden size: 9 tokens take the decode
-    # step kernels with h read from global memory (too many rows to cache),
-    # 12 tokens (120 pairs, below one 128-row chunk) the stream kernels
+    # mid-size dispatch on the full hidden size: the decode step kernels,
+    # with h read from global memory (too many rows to cache), at 9 tokens
+    # with 14 warps, at 12 with 12 warps and at 16 with 10 (x rows of the
+    # batch fill shared memory); 17 tokens (102 pairs at k = 6) the tensor
+    # cores with one chunk cut short
     inputs.Workload("dec_T9_H2560_I640_E32_k10", inputs.MoEShape(9, 2560, 640, 32, 10)),
-    inputs.Workload("stream_T12_H2560_I640_E32_k10", inputs.MoEShape(12, 2560, 640, 32, 10)),
+    inputs.Workload("dec_T12_H2560_I640_E32_k10", inputs.MoEShape(12, 2560, 640, 32, 10)),
+    inputs.Workload("dec_T16_H2560_I640_E32_k10", inputs.MoEShape(16, 2560, 640, 32, 10)),
+    inputs.Workload("tc_T17_H512_I128_E64_k6", inputs.MoEShape(17, 512, 128, 64, 6)),
 ]
 
 

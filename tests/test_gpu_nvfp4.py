@@ -104,22 +104,17 @@ def test_nvfp4_tensor_core_full_size_sampled(moe, wl):
     assert_close(layer.h.float().cpu().numpy()[row_of_pair[full_pairs]], rh, f"{wl.name} h rows")
 
 
-def test_nvfp4_stream_band_rejected_before_launch(moe):
-    """Shapes in the staged stream band (T > 16 and T*k < 128) have no NVFP4
-    kernel: every NVFP4 call returns MOE_ERR_UNSUPPORTED and writes nothing."""
-    sh = inputs.MoEShape(40, 256, 64, 8, 2)
-    assert moe.moe_step_kernel_path(sh.T, sh.E, sh.k, sh.H, sh.I) == moe.MOE_PATH_STREAM
-    logits, x = inputs.make_activations(sh.T, sh.H, sh.E, 0)
-    _, _, dw13, dw2 = weights_nvfp4(sh.E, sh.H, sh.I, 0)
-    layer = moe.MoELayerNvfp4(dw13, dw2, sh.T, sh.k)
-    layer.out.fill_(7.0)
-    lg, xx = torch.from_numpy(logits).cuda(), torch.from_numpy(x).cuda()
-    for fn in (layer.forward, layer.forward_layer):
-        with pytest.raises(moe.MoEError) as ei:
-            fn(lg, xx)
-        assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
-        torch.cuda.synchronize()
-        assert torch.all(layer.out == 7.0)
+@pytest.mark.parametrize("one_call", [False, True], ids=["steps", "one_call"])
+def test_nvfp4_between_decode_and_full_chunks(moe, one_call):
+    """T = 40, k = 2 (P = 80): past the decode kernels and short of one
+    128-row chunk, so the tensor cores run with chunks cut short."""
+    wl = inputs.Workload("mid_T40_H256_I64_E8_k2", inputs.MoEShape(40, 256, 64, 8, 2))
+    sh = wl.shape
+    assert moe.moe_step_kernel_path(sh.T, sh.E, sh.k, sh.H, sh.I) == moe.MOE_PATH_TENSOR_CORE
+    logits, x, w13, w2, layer, out = _layer(moe, wl, one_call)
+    ref = oracle.moe_forward_nvfp4(logits, x, w13, w2, sh.k)
+    assert np.array_equal(layer.topk_ids.cpu().numpy(), ref["topk_ids"])
+    assert_close(out.float().cpu().numpy(), ref["out"], f"{wl.name} out")
 
 
 def test_nvfp4_zero_expert_scale_zeroes_the_expert(moe):

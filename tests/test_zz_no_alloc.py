@@ -33,13 +33,16 @@ def moe():
     return m
 
 
-# One shape per kernel path of the down/combine step, each inside the 8 MiB
-# scratch: the decode kernels (fused combine), the staged stream kernels
-# (per-pair projections in the scratch, then the combine kernel) and the
-# tensor-core kernels (the same scratch areas through the tcgen05 path).
+# Shapes inside the 8 MiB scratch on each family the automatic choice takes
+# for the down/combine step: the decode kernels (fused combine; at 12 tokens
+# on the full hidden size with h read from global memory) and the
+# tensor-core kernels (per-pair projections in the scratch, then the combine
+# kernel), the latter with fewer sorted rows than one 128-row chunk (P = 102)
+# and with several chunks.
 SHAPES = [
     (inputs.MoEShape(4, 512, 128, 64, 6), "MOE_PATH_DECODE"),
-    (inputs.MoEShape(12, 2560, 640, 32, 10), "MOE_PATH_STREAM"),
+    (inputs.MoEShape(12, 2560, 640, 32, 10), "MOE_PATH_DECODE"),
+    (inputs.MoEShape(17, 512, 128, 64, 6), "MOE_PATH_TENSOR_CORE"),
     (inputs.MoEShape(64, 512, 128, 16, 4), "MOE_PATH_TENSOR_CORE"),
 ]
 

@@ -38,12 +38,15 @@ MOE_PATH_NONE = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_TENSOR_CORE = 2
 MOE_PATH_STREAM = 3
+MOE_PATH_AUTO = 0  # as an argument: the library's choice
 
 EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_step_kernel_path",
             "moe_get_device_error", "moe_topk_route", "moe_align_offsets", "moe_topk_route_align",
             "moe_w4a16_gate_up_silu", "moe_w4a16_down_combine",
             "moe_w4a16_down_combine_noalloc", "moe_layer_workspace_bytes", "moe_w4a16_moe_layer",
-            "moe_nvfp4_gate_up_silu", "moe_nvfp4_down_combine", "moe_nvfp4_moe_layer")
+            "moe_nvfp4_gate_up_silu", "moe_nvfp4_down_combine", "moe_nvfp4_moe_layer",
+            "moe_router_logits", "moe_router_route_align", "moe_awq_import",
+            "moe_w4a16_gate_up_silu_ex", "moe_w4a16_down_combine_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -90,6 +93,12 @@ def load_library(path: str = LIB_PATH):
         lib.moe_w4a16_down_combine.restype = _I
         lib.moe_w4a16_down_combine.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                _I, _I, _I, _I, _I, _P, _P, _SZ, _P]
+        lib.moe_w4a16_gate_up_silu_ex.restype = _I
+        lib.moe_w4a16_gate_up_silu_ex.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P,
+                                                  _I, _I, _I, _I, _I, _P, _P, _SZ, _I, _P]
+        lib.moe_w4a16_down_combine_ex.restype = _I
+        lib.moe_w4a16_down_combine_ex.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
+                                                  _I, _I, _I, _I, _I, _P, _P, _SZ, _I, _P]
         lib.moe_w4a16_down_combine_noalloc.restype = _I
         lib.moe_w4a16_down_combine_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                        _I, _I, _I, _I, _I, _P, _P]
@@ -107,6 +116,13 @@ def load_library(path: str = LIB_PATH):
         lib.moe_nvfp4_moe_layer.restype = _I
         lib.moe_nvfp4_moe_layer.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                             _P, _P, _P, _P, _SZ, _P]
+        lib.moe_router_logits.restype = _I
+        lib.moe_router_logits.argtypes = [_P, _P, _I, _I, _I, _P, _P, _SZ, _P]
+        lib.moe_router_route_align.restype = _I
+        lib.moe_router_route_align.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                               _P, _SZ, _P]
+        lib.moe_awq_import.restype = _I
+        lib.moe_awq_import.argtypes = [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _I, _I, _P]
         _lib = lib
         return lib
 
@@ -251,8 +267,10 @@ def moe_topk_route_align(logits, k: int, workspace=None, topk_ids=None, topk_w=N
     return topk_ids, topk_w, meta
 
 
-def moe_w4a16_gate_up_silu(x, w13, meta, k: int, workspace, h=None, stream=None, group_size=32):
-    """h[T*k, I] (fp16, sorted-row order).  w13 = (qweight, scales, qzeros)."""
+def moe_w4a16_gate_up_silu(x, w13, meta, k: int, workspace, h=None, stream=None, group_size=32,
+                           path=MOE_PATH_AUTO):
+    """h[T*k, I] (fp16, sorted-row order).  w13 = (qweight, scales, qzeros);
+    path forces a kernel family (MOE_PATH_*; AUTO: the library's choice)."""
     import torch
     q, s, z = w13
     T, H = x.shape
@@ -261,17 +279,23 @@ def moe_w4a16_gate_up_silu(x, w13, meta, k: int, workspace, h=None, stream=None,
     offs, sp, act, na = meta
     if h is None:
         h = torch.empty((T * k, I), dtype=torch.float16, device=x.device)
-    _check("moe_w4a16_gate_up_silu", load_library().moe_w4a16_gate_up_silu(
-        _dev(x, torch.float16, "x"), _dev(q, torch.int32, "w13_q"), _dev(s, torch.float16, "w13_s"),
-        _dev(z, torch.int32, "w13_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
-        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
-        _dev(na, torch.int32, "num_active"), T, E, k, H, I, _dev(h, torch.float16, "h"),
-        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    lib = load_library()
+    args = (_dev(x, torch.float16, "x"), _dev(q, torch.int32, "w13_q"), _dev(s, torch.float16, "w13_s"),
+            _dev(z, torch.int32, "w13_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
+            _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+            _dev(na, torch.int32, "num_active"), T, E, k, H, I, _dev(h, torch.float16, "h"),
+            _dev(workspace, torch.uint8, "workspace"), workspace.numel())
+    if path == MOE_PATH_AUTO:
+        _check("moe_w4a16_gate_up_silu", lib.moe_w4a16_gate_up_silu(*args, _stream(stream)))
+    else:
+        _check("moe_w4a16_gate_up_silu_ex", lib.moe_w4a16_gate_up_silu_ex(*args, path, _stream(stream)))
     return h
 
 
-def moe_w4a16_down_combine(h, w2, meta, topk_w, workspace, out=None, stream=None, group_size=32):
-    """out[T, H] (fp16).  w2 = (qweight, scales, qzeros)."""
+def moe_w4a16_down_combine(h, w2, meta, topk_w, workspace, out=None, stream=None, group_size=32,
+                           path=MOE_PATH_AUTO):
+    """out[T, H] (fp16).  w2 = (qweight, scales, qzeros); path as for
+    moe_w4a16_gate_up_silu."""
     import torch
     q, s, z = w2
     E, H, _ = q.shape
@@ -280,13 +304,17 @@ def moe_w4a16_down_combine(h, w2, meta, topk_w, workspace, out=None, stream=None
     offs, sp, act, na = meta
     if out is None:
         out = torch.empty((T, H), dtype=torch.float16, device=h.device)
-    _check("moe_w4a16_down_combine", load_library().moe_w4a16_down_combine(
-        _dev(h, torch.float16, "h"), _dev(q, torch.int32, "w2_q"), _dev(s, torch.float16, "w2_s"),
-        _dev(z, torch.int32, "w2_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
-        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
-        _dev(na, torch.int32, "num_active"), _dev(topk_w, torch.float32, "topk_w"),
-        T, E, k, H, I, _dev(out, torch.float16, "out"),
-        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    lib = load_library()
+    args = (_dev(h, torch.float16, "h"), _dev(q, torch.int32, "w2_q"), _dev(s, torch.float16, "w2_s"),
+            _dev(z, torch.int32, "w2_z"), group_size, _dev(offs, torch.int32, "expert_offsets"),
+            _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+            _dev(na, torch.int32, "num_active"), _dev(topk_w, torch.float32, "topk_w"),
+            T, E, k, H, I, _dev(out, torch.float16, "out"),
+            _dev(workspace, torch.uint8, "workspace"), workspace.numel())
+    if path == MOE_PATH_AUTO:
+        _check("moe_w4a16_down_combine", lib.moe_w4a16_down_combine(*args, _stream(stream)))
+    else:
+        _check("moe_w4a16_down_combine_ex", lib.moe_w4a16_down_combine_ex(*args, path, _stream(stream)))
     return out
 
 
@@ -402,6 +430,72 @@ def moe_nvfp4_moe_layer(logits, x, w13, w2, k: int, workspace, topk_ids=None, to
     return out, topk_ids, topk_w
 
 
+def moe_router_logits(x, w_router, logits=None, workspace=None, stream=None):
+    """logits [T, E] (fp32) = x [T, H] (fp16) times w_router [E, H] (fp16) transposed."""
+    import torch
+    T, H = x.shape
+    E = w_router.shape[0]
+    if w_router.shape[1] != H:
+        raise ValueError("w_router must be [E, H]")
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    ws = _dev(workspace, torch.uint8, "workspace") if workspace is not None else None
+    _check("moe_router_logits", load_library().moe_router_logits(
+        _dev(x, torch.float16, "x"), _dev(w_router, torch.float16, "w_router"), T, E, H,
+        _dev(logits, torch.float32, "logits"), ws, workspace.numel() if workspace is not None else 0,
+        _stream(stream)))
+    return logits
+
+
+def moe_router_route_align(x, w_router, k: int, workspace, logits=None, topk_ids=None, topk_w=None,
+                           meta=None, stream=None):
+    """Router logits, top-k routing and grouping in one call; returns
+    (logits, topk_ids, topk_w, (offsets, sorted_pair, active, num_active))."""
+    import torch
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if topk_w is None:
+        topk_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if meta is None:
+        meta = (torch.empty(E + 1, dtype=torch.int32, device=dev), torch.empty(T * k, dtype=torch.int32, device=dev),
+                torch.empty(E, dtype=torch.int32, device=dev), torch.empty(1, dtype=torch.int32, device=dev))
+    offs, sp, act, na = meta
+    _check("moe_router_route_align", load_library().moe_router_route_align(
+        _dev(x, torch.float16, "x"), _dev(w_router, torch.float16, "w_router"), T, E, k, H,
+        _dev(logits, torch.float32, "logits"), _dev(topk_ids, torch.int32, "topk_ids"),
+        _dev(topk_w, torch.float32, "topk_w"), _dev(offs, torch.int32, "expert_offsets"),
+        _dev(sp, torch.int32, "sorted_pair"), _dev(act, torch.int32, "active_experts"),
+        _dev(na, torch.int32, "num_active"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
+    return logits, topk_ids, topk_w, meta
+
+
+def moe_awq_import(awq, dst, row0: int = 0, stream=None):
+    """Repacks an AWQ GEMM-layout layer stack awq = (qweight [E][K][N/8],
+    qzeros [E][K/32][N/8], scales [E][K/32][N]) into rows [row0, row0+N) of
+    dst = (qweight [E][Ndst][K/8], scales [E][Ndst][K/32], qzeros
+    [E][Ndst/8][K/32]), in place on the device; returns dst."""
+    import torch
+    aq, az, as_ = awq
+    q, s, z = dst
+    E, K, N8 = aq.shape
+    Ndst = q.shape[1]
+    if q.shape != (E, Ndst, K // 8) or s.shape != (E, Ndst, K // 32) or z.shape != (E, Ndst // 8, K // 32):
+        raise ValueError("destination shapes do not match the AWQ layer")
+    if az.shape != (E, K // 32, N8) or as_.shape != (E, K // 32, N8 * 8):
+        raise ValueError("AWQ qzeros / scales shapes do not match qweight")
+    _check("moe_awq_import", load_library().moe_awq_import(
+        _dev(aq, torch.int32, "awq_qweight"), _dev(az, torch.int32, "awq_qzeros"),
+        _dev(as_, torch.float16, "awq_scales"), E, K, N8 * 8, 32, _dev(q, torch.int32, "qweight"),
+        _dev(s, torch.float16, "scales"), _dev(z, torch.int32, "qzeros"), Ndst, row0, _stream(stream)))
+    return dst
+
+
 def to_device_weights_nvfp4(w, device="cuda"):
     """(codes u32, bscale u8, gscale f32) numpy arrays -> CUDA tensors (codes viewed as int32)."""
     import numpy as np
@@ -426,9 +520,9 @@ class MoELayer:
     """Device weights plus preallocated buffers for one (T, E, k, H, I) shape;
     ``forward`` issues the four calls on one stream."""
 
-    def __init__(self, w13, w2, T: int, k: int, device="cuda"):
+    def __init__(self, w13, w2, T: int, k: int, device="cuda", path=MOE_PATH_AUTO):
         import torch
-        self.w13, self.w2 = w13, w2
+        self.w13, self.w2, self.path = w13, w2, path
         E, twoI, H8 = w13[0].shape
         self.E, self.I, self.H, self.T, self.k = E, twoI // 2, H8 * 8, T, k
         dev = torch.device(device)
@@ -448,9 +542,9 @@ class MoELayer:
         moe_topk_route(logits, self.k, self.topk_ids, self.topk_w, stream=stream)
         moe_align_offsets(self.topk_ids, self.E, self.workspace, out=self.meta, stream=stream)
         moe_w4a16_gate_up_silu(x, self.w13, self.meta, self.k, self.workspace, h=self.h,
-                               stream=stream)
+                               stream=stream, path=self.path)
         moe_w4a16_down_combine(self.h, self.w2, self.meta, self.topk_w, self.workspace,
-                               out=self.out, stream=stream)
+                               out=self.out, stream=stream, path=self.path)
         return self.out
 
     def forward_layer(self, logits, x, stream=None):
@@ -494,10 +588,14 @@ class MoELayer:
         a_layer = (logits.data_ptr(), x.data_ptr(), q13, s13, z13, q2, s2, z2, 32, T, E, k, H, I,
                    self.topk_ids.data_ptr(), self.topk_w.data_ptr(), self.out.data_ptr(), ws, wsb, st)
         self.layer_call = call(lib.moe_w4a16_moe_layer, "moe_w4a16_moe_layer", a_layer)
+        if self.path != MOE_PATH_AUTO:
+            gu = call(lib.moe_w4a16_gate_up_silu_ex, "moe_w4a16_gate_up_silu_ex", a_gu[:-1] + (self.path, st))
+            dn = call(lib.moe_w4a16_down_combine_ex, "moe_w4a16_down_combine_ex", a_dn[:-1] + (self.path, st))
+        else:
+            gu = call(lib.moe_w4a16_gate_up_silu, "moe_w4a16_gate_up_silu", a_gu)
+            dn = call(lib.moe_w4a16_down_combine, "moe_w4a16_down_combine", a_dn)
         return (call(lib.moe_topk_route, "moe_topk_route", a_route),
-                call(lib.moe_align_offsets, "moe_align_offsets", a_align),
-                call(lib.moe_w4a16_gate_up_silu, "moe_w4a16_gate_up_silu", a_gu),
-                call(lib.moe_w4a16_down_combine, "moe_w4a16_down_combine", a_dn))
+                call(lib.moe_align_offsets, "moe_align_offsets", a_align), gu, dn)
 
 
 class MoELayerNvfp4(MoELayer):
@@ -540,6 +638,7 @@ class MoELayerNvfp4(MoELayer):
         ra = call(lib.moe_topk_route_align, "moe_topk_route_align",
                   (logits.data_ptr(), T, E, k, self.topk_ids.data_ptr(), self.topk_w.data_ptr(),
                    offs, sp, act, na, ws, wsb, st))
+        self.route_align_call = ra
         gu = call(lib.moe_nvfp4_gate_up_silu, "moe_nvfp4_gate_up_silu",
                   (x.data_ptr(), c13, b13, g13, offs, sp, act, na, T, E, k, H, I, self.h.data_ptr(),
                    ws, wsb, st))

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "dispatch_table.cuh"
 
 #define MOE_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -65,6 +66,16 @@ cudaError_t launch_decode_layer_nvfp4(const float *, const __half *, const uint3
                                       const float *, const uint32_t *, const uint8_t *, const float *, int, int,
                                       int, int, int, int32_t *, float *, __half *, __half *, float *, uint32_t *,
                                       uint32_t *, uint32_t *, uint32_t *, int, size_t, cudaStream_t);
+
+bool router_fusable(int, int, int, size_t);
+int router_path(int, int, int, size_t);
+cudaError_t launch_router_logits(const __half *, const __half *, int, int, int, float *, uint32_t *, int, size_t,
+                                 cudaStream_t);
+cudaError_t launch_router_route_align(const __half *, const __half *, int, int, int, int, float *, int32_t *,
+                                      float *, int32_t *, int32_t *, int32_t *, int32_t *, uint32_t *, int,
+                                      cudaStream_t);
+cudaError_t launch_awq_import(const uint32_t *, const uint32_t *, const uint16_t *, int, int, int, uint32_t *,
+                              uint16_t *, uint32_t *, int, int, cudaStream_t);
 
 namespace {
 
@@ -127,6 +138,50 @@ bool all_aligned(const Ps *...ps) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+bool path_supported(int path, int T, int E, int k, int H, int I, size_t smem) {
+    switch (path) {
+        case MOE_PATH_DECODE: return decode_supported(T, E, k, H, I, smem);
+        case MOE_PATH_TENSOR_CORE: return tc_supported(T, E, k, H, I, smem);
+        case MOE_PATH_STREAM: return true;
+        default: return false;
+    }
+}
+
+// The kernels of the step calls for a shape: the per-shape table's measured
+// choice where it has one (and the path can take the shape), else by shape
+// alone: the latency-first decode kernels up to 16 tokens while their
+// shared-memory layout fits (at 9 and 10 tokens on the Qwen4Exp geometry
+// 123 and 137 us through the step calls, against 216 and 231 us on the
+// tensor cores), then the tensor cores, the stream kernels only where
+// neither fits.  A forced path the shape cannot take is
+// MOE_ERR_UNSUPPORTED.
+constexpr int kRuleDecodeMaxT = 16;
+
+// NVFP4 weights: the decode kernels by the same rule, else the tensor cores
+// (no stream kernels for this format); MOE_PATH_NONE if neither fits.
+int nvfp4_path(int T, int E, int k, int H, int I, size_t smem) {
+    if (T <= kRuleDecodeMaxT && decode_supported(T, E, k, H, I, smem)) return MOE_PATH_DECODE;
+    if (tc_supported(T, E, k, H, I, smem)) return MOE_PATH_TENSOR_CORE;
+    return MOE_PATH_NONE;
+}
+int resolve_path(int *path, int T, int E, int k, int H, int I, size_t smem) {
+    if (*path != MOE_PATH_AUTO) {
+        if (*path != MOE_PATH_DECODE && *path != MOE_PATH_TENSOR_CORE && *path != MOE_PATH_STREAM)
+            return MOE_ERR_INVALID_ARG;
+        return path_supported(*path, T, E, k, H, I, smem) ? MOE_OK : MOE_ERR_UNSUPPORTED;
+    }
+    const int tp = tuned_path(T, E, k, H, I);
+    if (tp != MOE_PATH_AUTO && path_supported(tp, T, E, k, H, I, smem))
+        *path = tp;
+    else if (T <= kRuleDecodeMaxT && decode_supported(T, E, k, H, I, smem))
+        *path = MOE_PATH_DECODE;
+    else if (tc_supported(T, E, k, H, I, smem))
+        *path = MOE_PATH_TENSOR_CORE;
+    else
+        *path = MOE_PATH_STREAM;
+    return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -173,9 +228,8 @@ MOE_EXPORT int moe_step_kernel_path(int T, int E, int k, int H, int I) {
     if (T == 0) return MOE_PATH_NONE;
     DeviceInfo di;
     if (device_info(&di) != cudaSuccess) return MOE_PATH_NONE;
-    if (decode_supported(T, E, k, H, I, di.smem_optin)) return MOE_PATH_DECODE;
-    if (tc_supported(T, E, k, H, I, di.smem_optin)) return MOE_PATH_TENSOR_CORE;
-    return MOE_PATH_STREAM;
+    int path = MOE_PATH_AUTO;
+    return resolve_path(&path, T, E, k, H, I, di.smem_optin) == MOE_OK ? path : MOE_PATH_NONE;
 }
 
 MOE_EXPORT int moe_topk_route(const float *logits, int T, int E, int k, int32_t *topk_ids,
@@ -231,12 +285,12 @@ MOE_EXPORT int moe_topk_route_align(const float *logits, int T, int E, int k, in
                                     num_active, err, di.smem_optin, s));
 }
 
-MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
-                                      const uint16_t *w13_s, const uint32_t *w13_z, int group_size,
-                                      const int32_t *expert_offsets, const int32_t *sorted_pair,
-                                      const int32_t *active_experts, const int32_t *num_active,
-                                      int T, int E, int k, int H, int I, uint16_t *h,
-                                      void *workspace, size_t ws_bytes, void *stream) {
+MOE_EXPORT int moe_w4a16_gate_up_silu_ex(const uint16_t *x, const uint32_t *w13_q,
+                                         const uint16_t *w13_s, const uint32_t *w13_z, int group_size,
+                                         const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                         const int32_t *active_experts, const int32_t *num_active,
+                                         int T, int E, int k, int H, int I, uint16_t *h,
+                                         void *workspace, size_t ws_bytes, int path, void *stream) {
     int st = check_sizes(T, E, k, H, I);
     if (st != MOE_OK) return st;
     if ((st = check_group(group_size)) != MOE_OK) return st;
@@ -250,15 +304,13 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     uint32_t *err = static_cast<uint32_t *>(workspace) + kCtrlErrorWord;
-    // dispatch by shape only (thresholds measured): decode batches the
-    // latency-first kernels, batches that fill a 128-row chunk the tensor
-    // cores, the stream kernels in between
-    if (decode_supported(T, E, k, H, I, di.smem_optin))
+    if ((st = resolve_path(&path, T, E, k, H, I, di.smem_optin)) != MOE_OK) return st;
+    if (path == MOE_PATH_DECODE)
         return cuda_status(launch_gate_up_decode(
             reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,
             expert_offsets, sorted_pair, active_experts, num_active, T, E, k, H, I,
             reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
-    if (tc_supported(T, E, k, H, I, di.smem_optin))
+    if (path == MOE_PATH_TENSOR_CORE)
         return cuda_status(launch_gate_up_tc(
             reinterpret_cast<const __half *>(x), w13_q, reinterpret_cast<const __half *>(w13_s), w13_z,
             expert_offsets, sorted_pair, active_experts, num_active, T, E, k, H, I,
@@ -272,6 +324,17 @@ MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
                               reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin,
                               static_cast<cudaStream_t>(stream));
     return cuda_status(e);
+}
+
+MOE_EXPORT int moe_w4a16_gate_up_silu(const uint16_t *x, const uint32_t *w13_q,
+                                      const uint16_t *w13_s, const uint32_t *w13_z, int group_size,
+                                      const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                      const int32_t *active_experts, const int32_t *num_active,
+                                      int T, int E, int k, int H, int I, uint16_t *h,
+                                      void *workspace, size_t ws_bytes, void *stream) {
+    return moe_w4a16_gate_up_silu_ex(x, w13_q, w13_s, w13_z, group_size, expert_offsets, sorted_pair,
+                                     active_experts, num_active, T, E, k, H, I, h, workspace, ws_bytes,
+                                     MOE_PATH_AUTO, stream);
 }
 
 namespace moe {
@@ -293,13 +356,13 @@ int check_down_combine_args(const uint16_t *h, const uint32_t *w2_q, const uint1
 }
 }  // namespace moe
 
-MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
-                                      const uint32_t *w2_z, int group_size,
-                                      const int32_t *expert_offsets, const int32_t *sorted_pair,
-                                      const int32_t *active_experts, const int32_t *num_active,
-                                      const float *topk_w, int T, int E, int k, int H, int I,
-                                      uint16_t *out, void *workspace, size_t ws_bytes,
-                                      void *stream) {
+MOE_EXPORT int moe_w4a16_down_combine_ex(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
+                                         const uint32_t *w2_z, int group_size,
+                                         const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                         const int32_t *active_experts, const int32_t *num_active,
+                                         const float *topk_w, int T, int E, int k, int H, int I,
+                                         uint16_t *out, void *workspace, size_t ws_bytes, int path,
+                                         void *stream) {
     int st = check_down_combine_args(h, w2_q, w2_s, w2_z, group_size, expert_offsets, sorted_pair,
                                      active_experts, num_active, topk_w, T, E, k, H, I, out);
     if (st != MOE_OK) return st;
@@ -312,14 +375,15 @@ MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, c
     const WorkspaceLayout L = workspace_layout(T, k, H);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
-    if (decode_supported(T, E, k, H, I, di.smem_optin))
+    if ((st = resolve_path(&path, T, E, k, H, I, di.smem_optin)) != MOE_OK) return st;
+    if (path == MOE_PATH_DECODE)
         return cuda_status(launch_down_decode(
             reinterpret_cast<const __half *>(h), w2_q, reinterpret_cast<const __half *>(w2_s), w2_z,
             expert_offsets, sorted_pair, active_experts, num_active, topk_w, T, E, k, H, I,
             reinterpret_cast<__half *>(out), reinterpret_cast<float *>(ws + L.y),
             reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms, di.smem_optin,
             static_cast<cudaStream_t>(stream)));
-    if (tc_supported(T, E, k, H, I, di.smem_optin))
+    if (path == MOE_PATH_TENSOR_CORE)
         return cuda_status(launch_down_tc(
             reinterpret_cast<const __half *>(h), w2_q, reinterpret_cast<const __half *>(w2_s), w2_z,
             expert_offsets, sorted_pair, active_experts, num_active, topk_w, T, E, k, H, I,
@@ -332,6 +396,18 @@ MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, c
                            reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms,
                            di.smem_optin, static_cast<cudaStream_t>(stream));
     return cuda_status(e);
+}
+
+MOE_EXPORT int moe_w4a16_down_combine(const uint16_t *h, const uint32_t *w2_q, const uint16_t *w2_s,
+                                      const uint32_t *w2_z, int group_size,
+                                      const int32_t *expert_offsets, const int32_t *sorted_pair,
+                                      const int32_t *active_experts, const int32_t *num_active,
+                                      const float *topk_w, int T, int E, int k, int H, int I,
+                                      uint16_t *out, void *workspace, size_t ws_bytes,
+                                      void *stream) {
+    return moe_w4a16_down_combine_ex(h, w2_q, w2_s, w2_z, group_size, expert_offsets, sorted_pair,
+                                     active_experts, num_active, topk_w, T, E, k, H, I, out, workspace,
+                                     ws_bytes, MOE_PATH_AUTO, stream);
 }
 
 namespace moe {
@@ -431,11 +507,12 @@ MOE_EXPORT int moe_nvfp4_gate_up_silu(const uint16_t *x, const uint32_t *w13_cod
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     uint32_t *err = static_cast<uint32_t *>(workspace) + kCtrlErrorWord;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_supported(T, E, k, H, I, di.smem_optin))
+    const int path = nvfp4_path(T, E, k, H, I, di.smem_optin);
+    if (path == MOE_PATH_DECODE)
         return cuda_status(launch_gate_up_decode_nvfp4(
             reinterpret_cast<const __half *>(x), w13_codes, w13_bscale, w13_gscale, expert_offsets, sorted_pair,
             active_experts, num_active, T, E, k, H, I, reinterpret_cast<__half *>(h), err, di.sms, di.smem_optin, s));
-    if (tc_supported(T, E, k, H, I, di.smem_optin))
+    if (path == MOE_PATH_TENSOR_CORE)
         return cuda_status(launch_gate_up_tc_nvfp4(
             reinterpret_cast<const __half *>(x), w13_codes, w13_bscale, w13_gscale, expert_offsets, sorted_pair,
             active_experts, num_active, T, E, k, H, I, reinterpret_cast<__half *>(h),
@@ -464,13 +541,14 @@ MOE_EXPORT int moe_nvfp4_down_combine(const uint16_t *h, const uint32_t *w2_code
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws) + kCtrlErrorWord;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (decode_supported(T, E, k, H, I, di.smem_optin))
+    const int path = nvfp4_path(T, E, k, H, I, di.smem_optin);
+    if (path == MOE_PATH_DECODE)
         return cuda_status(launch_down_decode_nvfp4(
             reinterpret_cast<const __half *>(h), w2_codes, w2_bscale, w2_gscale, expert_offsets, sorted_pair,
             active_experts, num_active, topk_w, T, E, k, H, I, reinterpret_cast<__half *>(out),
             reinterpret_cast<float *>(ws + L.y), reinterpret_cast<uint32_t *>(ws + L.counters), err, di.sms,
             di.smem_optin, s));
-    if (tc_supported(T, E, k, H, I, di.smem_optin))
+    if (path == MOE_PATH_TENSOR_CORE)
         return cuda_status(launch_down_tc_nvfp4(
             reinterpret_cast<const __half *>(h), w2_codes, w2_bscale, w2_gscale, expert_offsets, sorted_pair,
             active_experts, num_active, topk_w, T, E, k, H, I, reinterpret_cast<__half *>(out),
@@ -510,7 +588,7 @@ MOE_EXPORT int moe_nvfp4_moe_layer(const float *logits, const uint16_t *x, const
     int32_t *active = reinterpret_cast<int32_t *>(ws + L.active);
     int32_t *num_active = reinterpret_cast<int32_t *>(ws + L.num_active);
     uint16_t *h = reinterpret_cast<uint16_t *>(ws + L.h);
-    if (!decode_supported(T, E, k, H, I, di.smem_optin) && !tc_supported(T, E, k, H, I, di.smem_optin))
+    if (nvfp4_path(T, E, k, H, I, di.smem_optin) == MOE_PATH_NONE)
         return MOE_ERR_UNSUPPORTED;  // checked before anything is launched
     if ((st = moe_topk_route_align(logits, T, E, k, topk_ids, topk_w, offsets, sorted, active, num_active,
                                    workspace, ws_bytes, stream)) != MOE_OK)
@@ -520,4 +598,64 @@ MOE_EXPORT int moe_nvfp4_moe_layer(const float *logits, const uint16_t *x, const
         return st;
     return moe_nvfp4_down_combine(h, w2_codes, w2_bscale, w2_gscale, offsets, sorted, active, num_active, topk_w,
                                   T, E, k, H, I, out, workspace, ws_bytes, stream);
+}
+
+
+// ---------------------------------------------------------------- router logits
+MOE_EXPORT int moe_router_logits(const uint16_t *x, const uint16_t *w_router, int T, int E, int H, float *logits,
+                                 void *workspace, size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, 1, H, -1);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(w_router)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !all_aligned(x, logits)) return MOE_ERR_INVALID_ARG;
+    if (workspace && (ws_bytes < kCtrlBytes || !aligned16(workspace))) return MOE_ERR_WORKSPACE;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (router_path(T, E, H, di.smem_optin) == 0) return MOE_ERR_UNSUPPORTED;
+    uint32_t *err = workspace ? static_cast<uint32_t *>(workspace) + kCtrlErrorWord : nullptr;
+    return cuda_status(launch_router_logits(reinterpret_cast<const __half *>(x),
+                                            reinterpret_cast<const __half *>(w_router), T, E, H, logits, err,
+                                            di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_router_route_align(const uint16_t *x, const uint16_t *w_router, int T, int E, int k, int H,
+                                      float *logits, int32_t *topk_ids, float *topk_w, int32_t *expert_offsets,
+                                      int32_t *sorted_pair, int32_t *active_experts, int32_t *num_active,
+                                      void *workspace, size_t ws_bytes, void *stream) {
+    int st = check_sizes(T, E, k, H, -1);
+    if (st != MOE_OK) return st;
+    if (!all_aligned(w_router, expert_offsets, active_experts, num_active)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && !all_aligned(x, logits, topk_ids, topk_w, sorted_pair)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < kCtrlBytes || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+    DeviceInfo di;
+    cudaError_t e = device_info(&di);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T > 0 && router_fusable(T, E, k, di.smem_optin))
+        return cuda_status(launch_router_route_align(
+            reinterpret_cast<const __half *>(x), reinterpret_cast<const __half *>(w_router), T, E, k, H, logits,
+            topk_ids, topk_w, expert_offsets, sorted_pair, active_experts, num_active,
+            static_cast<uint32_t *>(workspace), di.sms, s));
+    if (T > 0 && router_path(T, E, H, di.smem_optin) == 0) return MOE_ERR_UNSUPPORTED;
+    if ((st = moe_router_logits(x, w_router, T, E, H, logits, workspace, ws_bytes, stream)) != MOE_OK) return st;
+    return moe_topk_route_align(logits, T, E, k, topk_ids, topk_w, expert_offsets, sorted_pair, active_experts,
+                                num_active, workspace, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------- AWQ import
+MOE_EXPORT int moe_awq_import(const uint32_t *awq_qweight, const uint32_t *awq_qzeros,
+                              const uint16_t *awq_scales, int E, int K, int N, int group_size,
+                              uint32_t *qweight, uint16_t *scales, uint32_t *qzeros, int N_dst, int row0,
+                              void *stream) {
+    if (E <= 0 || K <= 0 || N <= 0 || K % 32 || N % 8 || N_dst <= 0 || N_dst % 8 || row0 < 0 || row0 % 8 ||
+        (long long)row0 + N > N_dst)
+        return MOE_ERR_INVALID_ARG;
+    int st = check_group(group_size);
+    if (st != MOE_OK) return st;
+    if (E > kMaxE || K > kMaxDim || N_dst > 2 * kMaxDim) return MOE_ERR_UNSUPPORTED;
+    if (!all_aligned(awq_qweight, awq_qzeros, awq_scales, qweight, scales, qzeros)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_awq_import(awq_qweight, awq_qzeros, awq_scales, E, K, N, qweight, scales, qzeros,
+                                         N_dst, row0, static_cast<cudaStream_t>(stream)));
 }

@@ -18,6 +18,7 @@ constexpr int kCtrlErrorWord = 0;     // u32: MOE_DEVERR_* bits
 constexpr int kCtrlWaitPolls = MOE_CTRL_WAIT_POLLS;  // u32: polls before a cross-CTA wait gives up
 constexpr int kCtrlWaitExtra = MOE_CTRL_WAIT_EXTRA;  // u32: added to every cross-CTA wait target
 constexpr int kCtrlTimeline = MOE_CTRL_TIMELINE;     // u64 (words 4-5): timeline buffer address
+constexpr int kCtrlRouterTicket = 8;  // u32: CTAs of the fused router launch that have finished (0 between calls)
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -8,7 +8,9 @@
 // matters is how soon every SM has its share in flight and how many
 // independent instructions each warp can issue:
 //
-//  * One 14-warp CTA per SM.  A prologue, run by every thread with all loads
+//  * One CTA per SM, of 14 warps (fewer, down to 6, when step 3's cache of
+//    every x row leaves too little room for 14 task buffers: on the
+//    Qwen4Exp geometry 12 warps at 11-15 tokens, 10 at 16).  A prologue, run by every thread with all loads
 //    issued before any store, brings the routing metadata (active list,
 //    offsets, pair ids) and the activations (every x row in step 3, every h
 //    row in step 4 when they fit) into shared memory in a single round trip.
@@ -41,11 +43,12 @@ namespace moe {
 
 constexpr int kDecWarps = 14;
 constexpr int kDecThreads = kDecWarps * 32;
-// decode batches: T <= kDecMaxT when the layout fits in shared memory (on
-// the Qwen4Exp geometry up to 10 tokens: at 9 tokens these kernels take
-// 136 us against 297 us for the stream kernels)
+constexpr int kDecMinWarps = 6;
+// batches these kernels can take: T <= kDecMaxT when the layout fits in
+// shared memory (on the Qwen4Exp geometry, with fewer warps past 10 tokens,
+// up to 29).  Which batches they are chosen for is the dispatch's business.
 #ifndef DEC_MAX_T
-#define DEC_MAX_T 16
+#define DEC_MAX_T 32
 #endif
 constexpr int kDecMaxT = DEC_MAX_T;
 
@@ -76,15 +79,26 @@ struct DecLayout {
     uint32_t meta, blk, xc, wbuf, bars, total;
 };
 
-__host__ __device__ inline DecLayout dec_layout(int E, int P, int nblk, int slots, int K, uint32_t wbytes) {
+__host__ __device__ inline DecLayout dec_layout(int E, int P, int nblk, int slots, int K, uint32_t wbytes,
+                                                 int nw = kDecWarps) {
     DecLayout L;
     L.meta = 0;
     L.blk = (uint32_t)align_up((size_t)(4 + E + E + 1 + P) * 4, 128);
     L.xc = L.blk + (uint32_t)align_up((size_t)(2 * nblk + 4) * 4, 128);
     L.wbuf = L.xc + (uint32_t)align_up((size_t)slots * K * 2, 128);
-    L.bars = L.wbuf + (uint32_t)kDecWarps * wbytes;
-    L.total = L.bars + kDecWarps * 8;
+    L.bars = L.wbuf + (uint32_t)nw * wbytes;
+    L.total = L.bars + nw * 8;
     return L;
+}
+
+// Warps of a decode launch: kDecWarps, else the most of 12, 10, 8 or 6 whose
+// task buffers fit beside the activation cache (step 3 keeps every x row of
+// the batch, so larger batches leave room for fewer buffers); 0 if none fits.
+__host__ __device__ inline int dec_warps(int E, int P, int nblk, int slots, int K, uint32_t wbytes,
+                                         size_t smem_limit) {
+    for (int nw = kDecWarps; nw >= kDecMinWarps; nw -= 2)
+        if (dec_layout(E, P, nblk, slots, K, wbytes, nw).total <= smem_limit) return nw;
+    return 0;
 }
 
 // End of a token pass: finish the dot products across the L lanes of each
@@ -141,7 +155,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
     extern __shared__ __align__(128) uint8_t smem[];
     const int G = GT ? GT : a.K / 32;
     const int K = 32 * G;
-    const DecLayout Ly = dec_layout(a.E, a.P, a.nblk, a.slots, K, a.wbytes);
+    // warps of this launch (kDecWarps, or fewer where their buffers and a
+    // larger activation cache would not fit together)
+    const int NW = blockDim.x >> 5, NTH = NW * 32;
+    const DecLayout Ly = dec_layout(a.E, a.P, a.nblk, a.slots, K, a.wbytes, NW);
     const WarpGeom wg = warp_geom(Tr::RT, nmat, K);
     int *s_meta = reinterpret_cast<int *>(smem + Ly.meta);
     int *s_active = s_meta + 4;
@@ -157,18 +174,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         mbar_init(bar, 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < 2 * a.nblk + 1; i += kDecThreads) s_blk[i] = 0;
+    for (int i = tid; i < 2 * a.nblk + 1; i += NTH) s_blk[i] = 0;
     pdl_wait();
     pdl_trigger();
 
     // ---- prologue: metadata and activations, all loads first
     {
         const int nmeta = a.E + (a.E + 1) + a.P;  // active | offsets | pairs
-        for (int base = 0; base < nmeta; base += 4 * kDecThreads) {
+        for (int base = 0; base < nmeta; base += 4 * NTH) {
             int v[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int i = base + tid + c * kDecThreads;
+                const int i = base + tid + c * NTH;
                 v[c] = 0;
                 if (i < a.E)
                     v[c] = __ldg(a.active + i);
@@ -179,13 +196,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int i = base + tid + c * kDecThreads;
+                const int i = base + tid + c * NTH;
                 if (i < nmeta) s_active[i] = v[c];  // active, offsets, pairs are contiguous
             }
         }
         if (tid == 0) s_meta[0] = __ldg(a.num_active);
         // step 3: every x row; step 4: every h row when the cache holds them
-        if (MODE == kDecGateUp || a.slots >= a.P) dec_stage_rows(a.vin, MODE == kDecGateUp ? a.T : a.P, K, G, xcb, tid, kDecThreads);
+        if (MODE == kDecGateUp || a.slots >= a.P) dec_stage_rows(a.vin, MODE == kDecGateUp ? a.T : a.P, K, G, xcb, tid, NTH);
     }
     __syncthreads();
     const bool hc = MODE == kDecDown && a.slots >= a.P;
@@ -196,7 +213,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
     const int TPE = (a.rows + Tr::RT - 1) / Tr::RT;  // tasks per expert
     const int U = A * TPE;
     // tasks dealt round-robin: CTA first, then warp
-    const int ustride = gridDim.x * kDecWarps;
+    const int ustride = gridDim.x * NW;
     int u = blockIdx.x + gridDim.x * warp;
 
     // task u's expert and segment; false if the metadata is bad
@@ -306,7 +323,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         // atomic.  A thread whose atomic completes a block queues it.
         __syncthreads();
         int *s_done = s_blk + a.nblk, *s_ndone = s_blk + 2 * a.nblk;
-        for (int nb = tid; nb < a.nblk; nb += kDecThreads) {
+        for (int nb = tid; nb < a.nblk; nb += NTH) {
             const int cnt = s_blk[nb];
             if (cnt == 0 || dead) continue;
             __threadfence();
@@ -320,7 +337,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeArgs
         const int ndone = *s_ndone;
         if (ndone > 0) __threadfence();
         // each completed block: out[t][8 rows] = sum_j w[t][j] * y[t*k+j] in j order
-        for (int d = warp; d < ndone; d += kDecWarps) {
+        for (int d = warp; d < ndone; d += NW) {
             const int nb = s_done[d];
             for (int idx = lane; idx < a.T * 8; idx += 32) {
                 const int t = idx >> 3, n = nb * 8 + (idx & 7);
@@ -343,12 +360,13 @@ template <int MODE, int L, int RU, int GT, int FMT>
 inline cudaError_t launch_decode_t(DecodeArgs a, int num_sms, size_t smem_limit, cudaStream_t stream) {
     using Tr = DecTraits<MODE, L, RU>;
     a.wbytes = warp_geom(Tr::RT, Tr::nmat, a.K).bytes;
-    const size_t smem = dec_layout(a.E, a.P, a.nblk, a.slots, a.K, a.wbytes).total;
-    if (smem > smem_limit) return cudaErrorInvalidConfiguration;
+    const int nw = dec_warps(a.E, a.P, a.nblk, a.slots, a.K, a.wbytes, smem_limit);
+    if (nw == 0) return cudaErrorInvalidConfiguration;
+    const size_t smem = dec_layout(a.E, a.P, a.nblk, a.slots, a.K, a.wbytes, nw).total;
     static int configured[128];
     cudaError_t e = ensure_smem(decode_kernel<MODE, L, RU, GT, FMT>, configured, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(decode_kernel<MODE, L, RU, GT, FMT>, num_sms, kDecThreads, smem, stream, a);
+    return launch_pdl(decode_kernel<MODE, L, RU, GT, FMT>, num_sms, nw * 32, smem, stream, a);
 }
 
 // Lanes per row unit: a power of two giving each lane about five groups.
@@ -370,10 +388,9 @@ inline int down_slots(int T, int E, int k, int H, int I, size_t smem_limit) {
 
 inline bool decode_supported_impl(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int P = T * k;
-    return T >= 1 && T <= kDecMaxT &&
-           dec_layout(E, P, 0, T, H, decode_wbytes(H, I, true)).total <= smem_limit &&
-           dec_layout(E, P, H / 8, down_slots(T, E, k, H, I, smem_limit), I,
-                      decode_wbytes(H, I, false)).total <= smem_limit;
+    return T >= 1 && T <= kDecMaxT && dec_warps(E, P, 0, T, H, decode_wbytes(H, I, true), smem_limit) > 0 &&
+           dec_warps(E, P, H / 8, down_slots(T, E, k, H, I, smem_limit), I, decode_wbytes(H, I, false),
+                     smem_limit) > 0;
 }
 
 template <int FMT>

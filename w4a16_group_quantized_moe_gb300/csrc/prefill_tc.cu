@@ -44,6 +44,7 @@
 
 #include "align.cuh"
 #include "decode_common.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 
@@ -161,68 +162,6 @@ struct TcCtrl {
 __host__ __device__ inline size_t tc_smem_bytes(uint32_t a_bytes, int astages, uint32_t b_bytes, int bstages,
                                                 uint32_t c_bytes, int cstages) {
     return 1024 + (size_t)a_bytes * astages + (size_t)b_bytes * bstages + (size_t)c_bytes * cstages + sizeof(TcCtrl);
-}
-
-// ---------------------------------------------------------------- PTX
-__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
-    // shared-memory matrix descriptor: K-major, 128-byte swizzle; start
-    // address >> 4, leading offset unused (1), stride offset 1024 B between
-    // 8-row groups, descriptor version 1, layout type 2 (128-byte swizzle)
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24
-__device__ __forceinline__ uint32_t tc_idesc(int m, int n) {
-    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// L2 prefetch of one box of a tensor map (no shared memory, no completion)
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// byte offset of 16-byte chunk c (K elements 8c..8c+7) of row r in a
-// 128-byte-swizzled K-major tile
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
 // ---------------------------------------------------------------- work list
@@ -730,25 +669,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ---------------------------------------------------------------- host side
 namespace {
 
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-    static EncodeTiled fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(f);
-    }
-    return fn;
-}
-
 // 2-D map over the packed codes viewed as [E*N rows][K/8 words], box of
 // 8 words x 128 rows (one 64-wide K block of one tile); reads beyond the
 // tensor return zeros.
@@ -761,21 +681,6 @@ cudaError_t codes_map(CUtensorMap *map, const uint32_t *q, int E, int N, int K) 
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(q), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-// 2-D map over fp16 activation rows [rows][K] with the 128-byte swizzle;
-// box of 64 elements x box_rows rows.
-cudaError_t rows_map(CUtensorMap *map, const __half *base, long long rows, int K, int box_rows) {
-    EncodeTiled fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {kTcKB, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -807,7 +712,7 @@ cudaError_t launch_tc(const TcArgs &a0, const uint32_t *q, const __half *brows, 
     CUtensorMap map, bmap;
     cudaError_t e = codes_map(&map, q, a.E, a.N, a.K);
     if (e != cudaSuccess) return e;
-    e = rows_map(&bmap, brows, nbrows, a.K, kTcMaxN);
+    e = rows_map(&bmap, brows, nbrows, a.K, kTcKB, kTcMaxN);
     if (e != cudaSuccess) return e;
     static int configured[128];
     e = ensure_smem(tc_kernel<MODE, FMT>, configured, smem);
@@ -853,8 +758,9 @@ __global__ void sorted_rows_kernel(const uint4 *__restrict__ x, const int32_t *_
 // 32 (groups) and enough rows per expert on average to fill MMA granules.
 bool tc_supported(int T, int E, int k, int H, int I, size_t smem_limit) {
     const int amax = E < T * k ? E : T * k;
-    // P >= kTcMaxN: a chunk's activation box never reaches past the sorted rows' end
-    return T >= kTcMinT && T * k >= kTcMaxN && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
+    // a chunk's activation box may reach past the last sorted row (P < 128):
+    // those rows lie outside the tensor map and are read as zeros
+    return T >= kTcMinT && H % 32 == 0 && I % 32 == 0 && encode_fn() != nullptr &&
            tc_smem_bytes(TcGeom<kTcGateUp>::a_bytes, 2, TcGeom<kTcGateUp>::b_bytes, 2, TcGeom<kTcGateUp>::c_bytes,
                          TC_MIN_C_STAGES) + 16 + tc_table_bytes(amax) <=
                smem_limit;

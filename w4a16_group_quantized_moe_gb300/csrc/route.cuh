@@ -42,10 +42,17 @@ __device__ __forceinline__ void lane_best(const uint32_t (&key)[PER], uint32_t t
     bj = jj[0];
 }
 
+// A logit: through the read-only cache, or (FRESH: written earlier in the
+// same kernel by other CTAs) from L2.
+template <bool FRESH>
+__device__ __forceinline__ float load_logit(const float *p) {
+    return FRESH ? __ldcg(p) : __ldg(p);
+}
+
 // Routes one token with one warp.  PER = logits held per lane (E <= 32*PER).
 // Writes ids and weights of token t to every destination given (non-null):
 // topk_ids / topk_w at [t*k + j], and s_ids / s_w at [t*k + j].
-template <int PER>
+template <int PER, bool FRESH = false>
 __device__ __forceinline__ void route_token(const float *__restrict__ row, int E, int k, int t,
                                             int32_t *__restrict__ topk_ids, float *__restrict__ topk_w,
                                             int *s_ids, float *s_w = nullptr) {
@@ -54,7 +61,7 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
-        key[j] = e < E ? order_key(__ldg(row + e)) : 0u;
+        key[j] = e < E ? order_key(load_logit<FRESH>(row + e)) : 0u;
     }
     // this lane's best untaken candidate (first maximum in index order)
     uint32_t bk, taken = 0;
@@ -74,7 +81,7 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
     }
 
     // weights: softmax over the selected logits (rank 0 holds the maximum)
-    const float my_logit = lane < k ? __ldg(row + my_id) : 0.f;
+    const float my_logit = lane < k ? load_logit<FRESH>(row + my_id) : 0.f;
     const float m = __shfl_sync(0xffffffffu, my_logit, 0);
     const float ex = (lane < k) ? expf(my_logit - m) : 0.f;
     float sum = ex;
@@ -98,6 +105,7 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
 // lowest index), takes the warp maximum and, among lanes holding it, the
 // lowest expert index; the winner's key is cleared.  Results are identical
 // to route_token's.  E <= 1024.
+template <bool FRESH = false>
 __device__ __forceinline__ void route_token_compact(const float *__restrict__ row, int E, int k, int t,
                                                     int32_t *__restrict__ topk_ids,
                                                     float *__restrict__ topk_w, int *s_ids, float *s_w,
@@ -107,7 +115,7 @@ __device__ __forceinline__ void route_token_compact(const float *__restrict__ ro
         // every load first (one memory round trip), then the keys
         float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = lane + 32 * j < E ? __ldg(row + lane + 32 * j) : 0.f;
+        for (int j = 0; j < 32; ++j) v[j] = lane + 32 * j < E ? load_logit<FRESH>(row + lane + 32 * j) : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (lane + 32 * j < E) s_key[lane + 32 * j] = order_key(v[j]);
@@ -133,7 +141,7 @@ __device__ __forceinline__ void route_token_compact(const float *__restrict__ ro
         if (lane == (win & 31)) s_key[win] = 0u;
         __syncwarp();
     }
-    const float my_logit = lane < k ? __ldg(row + my_id) : 0.f;
+    const float my_logit = lane < k ? load_logit<FRESH>(row + my_id) : 0.f;
     const float m = __shfl_sync(0xffffffffu, my_logit, 0);
     const float ex = (lane < k) ? expf(my_logit - m) : 0.f;
     float sum = ex;

@@ -129,6 +129,24 @@ def make_workload(w: Workload, seed: int | None = None):
     return logits, x, w13, w2
 
 
+def make_router(E: int, H: int, seed: int = 0) -> np.ndarray:
+    """Router matrix w_router f16 [E, H] ~ N(0, 1/H): with x ~ N(0, 1) the
+    logits x . w_router[e] have unit variance, like the logits drawn above."""
+    w = _rng(seed, 51).standard_normal((E, H), dtype=np.float32) / np.float32(np.sqrt(H))
+    return w.astype(np.float16)
+
+
+def make_awq_layer(E: int, K: int, N: int, seed: int = 0, tag: int = 61):
+    """A stack of E AWQ GEMM-layout layers with input size K and output size
+    N: (qweight u32 [E][K][N/8], qzeros u32 [E][K/32][N/8], scales f16
+    [E][K/32][N]); codes and zeros uniformly random words, scales as above."""
+    if K % 32 or N % 8:
+        raise ValueError("K must be a multiple of 32 and N of 8")
+    return (_words(_rng(seed, tag), (E, K, N // 8)),
+            _words(_rng(seed, tag + 1), (E, K // 32, N // 8)),
+            _scales(_rng(seed, tag + 2), (E, K // 32, N)))
+
+
 def random_topk_ids(T: int, E: int, k: int, seed: int = 0) -> np.ndarray:
     """k distinct expert ids per token, uniformly at random (for testing the
     grouping step on its own)."""
