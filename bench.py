@@ -58,6 +58,8 @@ def parse():
                     help="comma-separated batch sizes: instead of the bench line, time the step calls on "
                          "every kernel family (and the one-call layer) at each T on the Qwen4Exp and TP4-shard "
                          "geometries, one JSON line per (geometry, T)")
+    ap.add_argument("--around-only", action="store_true",
+                    help="print only the router and AWQ-import figures (one JSON line)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the secondary per-workload figures")
     ap.add_argument("--layers", type=int, default=0,
@@ -351,7 +353,7 @@ def run_reference(args, wl):
 
 
 # sources the one-launch decode layer kernel is compiled from
-DECODE_LAYER_SOURCES = ("common.cuh", "route.cuh", "decode_layer.cuh", "decode_layer.cu")
+DECODE_LAYER_SOURCES = ("common.cuh", "decode_common.cuh", "route.cuh", "decode_layer.cuh", "decode_layer.cu")
 
 
 def source_digest() -> str:
@@ -569,6 +571,79 @@ NVFP4_CONFIG = ("qwen4exp_decode_T1_H2560_I640_E512_k10", "qwen4exp_decode_T2_H2
                 "qwen4exp_prefill_T4096_H2560_I640_E512_k10")
 
 
+def around_layer_figures(moe, dev):
+    """The steps on either side of the layer on the Qwen4Exp geometry, timed
+    with CUDA events on the launching stream (inputs larger than L2 where the
+    step reads much; means over the timed launches):
+    - moe_router_route_align at T = 1 and 8 (one launch: GEMV of the 2.6 MB
+      router matrix, top-k and grouping) and T = 4096 (tcgen05 GEMM, then
+      route and align); roofline: router-matrix bytes (HBM) for the GEMV,
+      2*T*E*H FLOPs (tensor) for the GEMM;
+    - moe_awq_import of a 512-expert gate layer (K 2560, N 640) into the
+      gate half of W13; roofline: bytes read + written (HBM)."""
+    import torch
+    from w4a16_group_quantized_moe_gb300 import inputs
+    E, H, I, k = 512, 2560, 640, 10
+    hbm, kind, _ = peaks()
+    tpk, tsrc = tensor_peak()
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    copies = 64  # router matrices used in turn: 168 MB, more than the L2 holds
+    wrs = [torch.from_numpy(inputs.make_router(E, H, seed=s)).to(dev) for s in range(copies)]
+    for T in (1, 8, 4096):
+        x = torch.from_numpy(inputs.make_activations(T, H, E, seed=T)[1]).to(dev)
+        ws = moe.new_workspace(T, E, k, 32, 32, device=dev)  # the router uses its control block only
+        bufs = moe.moe_router_route_align(x, wrs[0], k, ws)
+        n = 200 if T <= 8 else 30
+        for i in range(10):
+            moe.moe_router_route_align(x, wrs[i % copies], k, ws, *bufs[:3], meta=bufs[3])
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+        for i in range(n):
+            torch.cuda._sleep(100000)
+            ev[2 * i].record(stream)
+            moe.moe_router_route_align(x, wrs[i % copies], k, ws, *bufs[:3], meta=bufs[3])
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        if moe.moe_get_device_error(ws):
+            raise RuntimeError("device error in the router")
+        us = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n)]) * 1e3)
+        if T <= 16:
+            b = E * H * 2 + T * H * 2 + T * E * 4
+            roof = {"bound": "hbm", "achieved": b / us / 1e3, "peak": hbm, "unit": "GB/s",
+                    "frac": b / us / 1e3 / hbm, "bytes": b}
+        else:
+            f = 2.0 * T * E * H
+            roof = {"bound": "tensor", "achieved": f / us / 1e6, "peak": tpk, "unit": "TFLOP/s",
+                    "frac": f / us / 1e6 / tpk, "flops": f, "peak_source": tsrc}
+        out[f"router_route_align_T{T}"] = {"us": us, "launches": 1 if T <= 16 else 3, "roofline": roof}
+    del wrs
+    # AWQ import: two source stacks used in turn (1.9 GB together)
+    K, N = H, I
+    srcs = []
+    for s in range(2):
+        aq, az, as_ = inputs.make_awq_layer(E, K, N, seed=s)
+        srcs.append((torch.from_numpy(aq.view(np.int32)).to(dev), torch.from_numpy(az.view(np.int32)).to(dev),
+                     torch.from_numpy(as_).to(dev)))
+    dst = (torch.zeros((E, 2 * N, K // 8), dtype=torch.int32, device=dev),
+           torch.zeros((E, 2 * N, K // 32), dtype=torch.float16, device=dev),
+           torch.zeros((E, 2 * N // 8, K // 32), dtype=torch.int32, device=dev))
+    for i in range(3):
+        moe.moe_awq_import(srcs[i % 2], dst, 0)
+    n = 20
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    for i in range(n):
+        ev[2 * i].record(stream)
+        moe.moe_awq_import(srcs[i % 2], dst, 0)
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    us = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n)]) * 1e3)
+    b = 2 * (E * K * N // 2 + E * (K // 32) * N * 2 + E * (K // 32) * (N // 8) * 4)
+    out["awq_import_E512_K2560_N640"] = {"us": us, "launches": 1, "roofline": {
+        "bound": "hbm", "achieved": b / us / 1e3, "peak": hbm, "unit": "GB/s", "frac": b / us / 1e3 / hbm,
+        "bytes": b}}
+    return out
+
+
 SWEEP_GEOMS = (("qwen4exp", 2560, 640, 512, 10, (), 0.0),
                ("tp4shard", 2560, 160, 512, 10, tuple(range(16)), 2.0))
 
@@ -650,6 +725,9 @@ def main():
     if args.sweep_paths:
         sweep_paths(moe, dev, [int(t) for t in args.sweep_paths.split(",")])
         return
+    if args.around_only:
+        print(json.dumps({"around_layer": around_layer_figures(moe, dev)}))
+        return
 
     sh = wl.shape
     T, H, I, E, k = sh.T, sh.H, sh.I, sh.E, sh.k
@@ -726,7 +804,7 @@ def main():
             timeline = phase_timeline(moe, rig, args.timeline, dev)
         del rig
 
-        per_config = nvfp4 = mid = None
+        per_config = nvfp4 = mid = around = None
         if rank == 0 and not args.no_per_config:
             per_config = per_config_figures(moe, dev, geoms, [n for n in PER_CONFIG if n != wl.name],
                                             args.sets)
@@ -736,6 +814,9 @@ def main():
                     moe.moe_step_kernel_path(int(m["workload"].split("_T")[1].split("_")[0]), 512, 10, 2560, 640))
             nvfp4 = per_config_figures(moe, dev, lambda w: geoms(w, fmt="nvfp4"), NVFP4_CONFIG, args.sets,
                                        fmt="nvfp4")
+            geo_cache.clear()
+            torch.cuda.empty_cache()
+            around = around_layer_figures(moe, dev)
     geo_cache.clear()
 
     tot_ms = max_over_ranks(float(layer_ms.sum()), dev)
@@ -775,6 +856,7 @@ def main():
             "per_config": per_config,
             "nvfp4_per_config": nvfp4,
             "mid_size": mid,
+            "around_layer": around,
             "timeline": timeline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",

@@ -23,12 +23,12 @@ struct PathRange {
 //   Qwen4Exp (2560, 640, 512, 10):  T=9 123 / 216, 12 159 / 225, 16 219 / 272,
 //       17 234 / 276, 20 274 / 315, 24 343 / 359, 26 406 / 372, 28 443 / 400
 //   TP4 shard (2560, 160, 512, 10): T=9 75 / 100, 12 93 / 107, 16 109 / 134,
-//       17 117 / 138, 20 126 / 144, 24 146 / 147, 26 161 / 148, 28 167 / 152
+//       17 117 / 138, 20 126 / 144, 22 142 / 144, 24 149 / 148, 26 164 / 150
 constexpr PathRange kPathTable[] = {
     {2560, 640, 512, 10, 1, 24, MOE_PATH_DECODE},
     {2560, 640, 512, 10, 25, 1 << 24, MOE_PATH_TENSOR_CORE},
-    {2560, 160, 512, 10, 1, 24, MOE_PATH_DECODE},
-    {2560, 160, 512, 10, 25, 1 << 24, MOE_PATH_TENSOR_CORE},
+    {2560, 160, 512, 10, 1, 22, MOE_PATH_DECODE},
+    {2560, 160, 512, 10, 23, 1 << 24, MOE_PATH_TENSOR_CORE},
 };
 
 inline int tuned_path(int T, int E, int k, int H, int I) {
