@@ -102,13 +102,13 @@ def layer_launches(moe, T: int, E: int, k: int, H: int, I: int) -> int:
     family) and the kernel files:
     - decode batches that fit the one-launch layer (T <= 8): one cooperative
       kernel;
-    - otherwise route+align (one launch for T <= 32, else two), then
+    - otherwise route and align (two launches), then
       - decode kernels: gate/up, down with the combine fused (2);
       - tensor cores: x gather + gate/up, down + combine (4);
       - stream kernels: gate/up, down (+ the combine kernel above 8 tokens)."""
     if T <= 8:
         return 1
-    ra = 1 if T <= 32 else 2
+    ra = 2
     path = moe.moe_step_kernel_path(T, E, k, H, I)
     if path == moe.MOE_PATH_DECODE:
         return ra + 2

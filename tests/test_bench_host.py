@@ -50,9 +50,9 @@ def test_launch_count_follows_the_dispatch():
     assert bench.layer_launches(dec, 1, *q) == 1        # one cooperative kernel
     assert bench.layer_launches(tc, 8, *q) == 1
     assert bench.layer_launches(tc, 4096, *q) == 6      # route, align, gather, gate/up, down, combine
-    assert bench.layer_launches(tc, 32, *q) == 5        # route+align in one launch
-    assert bench.layer_launches(dec, 9, *q) == 3        # decode step kernels, combine fused
-    assert bench.layer_launches(st, 12, *q) == 4        # stream kernels + combine
+    assert bench.layer_launches(tc, 32, *q) == 6
+    assert bench.layer_launches(dec, 9, *q) == 4        # route, align, decode step kernels (combine fused)
+    assert bench.layer_launches(st, 12, *q) == 5        # route, align, stream kernels, combine
 
 
 def _rank_main(rank, port, q):

@@ -13,12 +13,18 @@
 // r = 8b + j holds the nibble of column j, which sits in slot
 // (j >> 1) | ((j & 1) << 2) of the AWQ word).
 //
-// One CTA per tile of 256 K rows x 64 output columns of one expert: it reads
-// the tile's 8 KB of codes (each K row's 32 contiguous bytes), the 8 groups
-// of scales and zeros, into shared memory, then writes each of the 64 output
-// rows' 128 contiguous bytes of codes (two 16-byte stores per thread), the
-// rows' scales and the 8 zero words.  Both sides move whole 32-byte sectors:
-// the kernel is a copy bound by HBM.
+// One CTA per tile of 256 K rows x 64 output columns of one expert.  Each
+// thread loads 8 code words: the same 8 columns (one AWQ word) on 8
+// consecutive K rows; as a matrix of nibbles (row = K row, column = word
+// slot) that is an 8x8 block, and its transpose is 8 words of the layer's
+// layout (word s = the 8 K codes of the column in slot s).  The transpose is
+// three rounds of masked shift/xor swaps between word pairs (blocks of 4,
+// 8 and 16 bits), about nine instructions per word, all in registers.  The
+// words go through a padded shared-memory tile so that each output row's
+// 128 contiguous bytes are written by one warp; scales (a 16-bit transpose)
+// take the same route, and each zero word is a nibble permutation of one
+// AWQ word.  Loads and stores move whole 32-byte sectors: the kernel is a
+// copy bound by HBM.
 #include "common.cuh"
 
 namespace moe {
@@ -38,8 +44,32 @@ struct AwqArgs {
     uint16_t *s;
 };
 
+// Transposes the 8x8 nibble matrix held in a[0..7] (a[i] nibble s ->
+// a[s] nibble i): swaps of 4-bit blocks between words i, i+1, of 8-bit
+// blocks between i, i+2, of 16-bit blocks between i, i+4.
+__device__ __forceinline__ void transpose_nibbles(uint32_t (&a)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint32_t x = ((a[i] >> 4) ^ a[i + 1]) & 0x0F0F0F0Fu;
+        a[i + 1] ^= x;
+        a[i] ^= x << 4;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += (i & 1) ? 3 : 1) {  // 0, 1, 4, 5
+        const uint32_t x = ((a[i] >> 8) ^ a[i + 2]) & 0x00FF00FFu;
+        a[i + 2] ^= x;
+        a[i] ^= x << 8;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t x = ((a[i] >> 16) ^ a[i + 4]) & 0x0000FFFFu;
+        a[i + 4] ^= x;
+        a[i] ^= x << 16;
+    }
+}
+
 __global__ void __launch_bounds__(kAwqThreads) awq_import_kernel(const AwqArgs a) {
-    __shared__ uint32_t t_codes[kAwqKT][kAwqNT / 8];
+    __shared__ uint32_t t_out[kAwqNT][kAwqKT / 8 + 1];  // [output row][output word], padded
     __shared__ uint16_t t_scales[kAwqKT / 32][kAwqNT];
     pdl_wait();
     pdl_trigger();
@@ -49,13 +79,21 @@ __global__ void __launch_bounds__(kAwqThreads) awq_import_kernel(const AwqArgs a
     const int W = a.N / 8, G = a.K / 32;
     const int c0 = n0 / 8, g0 = k0 / 32;
     const uint32_t *aq = a.aq + (size_t)e * a.K * W;
-    // codes: 8 words per K row, 4 rows per warp instruction
+    // codes: thread = (AWQ word cw of the tile, 8 K rows from 8 * kq)
+    {
+        const int cw = tid & 7, kq = tid >> 3;
+        const int kr = k0 + 8 * kq;
+        uint32_t v[8];
+        const bool ok = kr < a.K && c0 + cw < W;  // K is a multiple of 8: all 8 rows or none
 #pragma unroll
-    for (int i = 0; i < kAwqKT * (kAwqNT / 8) / kAwqThreads; ++i) {
-        const int idx = tid + i * kAwqThreads;
-        const int kr = idx >> 3, c = idx & 7;
-        const bool ok = k0 + kr < a.K && c0 + c < W;
-        t_codes[kr][c] = ok ? __ldg(aq + (size_t)(k0 + kr) * W + c0 + c) : 0u;
+        for (int i = 0; i < 8; ++i) v[i] = ok ? __ldg(aq + (size_t)(kr + i) * W + c0 + cw) : 0u;
+        transpose_nibbles(v);
+        // word s now holds the 8 codes of column 8 cw + ORDER[s]
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl) {
+            const int j = (sl & 3) * 2 + (sl >> 2);  // ORDER[sl]
+            t_out[8 * cw + j][kq] = v[sl];
+        }
     }
     // scales: 8 groups x 64 columns
 #pragma unroll
@@ -77,26 +115,14 @@ __global__ void __launch_bounds__(kAwqThreads) awq_import_kernel(const AwqArgs a
         }
     }
     __syncthreads();
-    // codes out: thread = (column n, quarter qq of the tile's 32 words per row)
+    // codes out: one warp per output row, lane = word of the row (128 bytes)
     {
-        const int n = tid & (kAwqNT - 1), qq = tid >> 6;
-        const int sl = awq_slot(n & 7), cw = n >> 3;
         const size_t KW = (size_t)a.K / 8;
-        const int kw0 = k0 / 8 + qq * 8;  // first output word of this thread
-        if (n0 + n < a.N && kw0 < (int)KW) {
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t v = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v |= ((t_codes[(qq * 8 + i) * 8 + j][cw] >> (4 * sl)) & 0xFu) << (4 * j);
-                o[i] = v;
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(a.q + ((size_t)e * a.Ndst + a.row0 + n0 + n) * KW + kw0);
-            // K is a multiple of 32, so the words left in a row come in fours
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            if (kw0 + 4 < (int)KW) dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        }
+        const int lane = tid & 31;
+        const int kw = k0 / 8 + lane;
+        for (int n = tid >> 5; n < kAwqNT; n += kAwqThreads / 32)
+            if (n0 + n < a.N && kw < (int)KW)
+                a.q[((size_t)e * a.Ndst + a.row0 + n0 + n) * KW + kw] = t_out[n][lane];
     }
     // scales out: 8 consecutive groups of each row
 #pragma unroll

@@ -7,13 +7,14 @@
 // Two kernels:
 //   router_gemv_kernel  decode batches (T <= 16).  The router matrix (2.6 MB
 //       at E = 512, H = 2560) is the only real traffic, so this is a GEMV
-//       bound by HBM and by latency: one warp per expert row, every lane's
-//       16-byte chunks of the row requested at once, the T activation
-//       chunks at the same K offsets read through L1 (every warp of the CTA
-//       reads the same x).  With `fused`, the last CTA to finish (found by an
-//       atomic ticket after a release fence; no CTA ever waits for another)
-//       also routes every token and groups the pairs, so logits, top-k and
-//       segments come out of one launch.
+//       bound by HBM and by latency: the CTA first stages the batch's x
+//       rows in shared memory (one round trip, every thread's loads in
+//       flight together), then one warp per expert row requests all of its
+//       lane's 16-byte chunks of the row at once and multiplies them by the
+//       T activation chunks at the same K offsets.  With `fused`, the last
+//       CTA to finish (found by an atomic ticket after a release fence; no
+//       CTA ever waits for another) also routes every token and groups the
+//       pairs, so logits, top-k and segments come out of one launch.
 //   router_tc_kernel    larger batches: a dense contraction on the tcgen05
 //       tensor cores.  One CTA per 128-token x 128-expert tile; warp 0 copies
 //       the x and router tiles of each 64-wide K block by TMA (128-byte
@@ -30,6 +31,7 @@ namespace moe {
 constexpr int kRgThreads = 256;  // GEMV block: 8 warps, one expert row each
 constexpr int kRgMaxT = 16;      // tokens the GEMV path takes
 constexpr int kRgChunks = 12;    // 16-byte row chunks a lane requests at once (H <= 3072 in one round)
+constexpr size_t kRgStageMax = 96 * 1024;  // x rows staged in shared memory up to this size
 
 // ---------------------------------------------------------------- GEMV
 __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
@@ -45,6 +47,24 @@ __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
     return s;
 }
 
+// x rows into shared memory, all loads issued before the stores
+__device__ __forceinline__ void stage_x(const uint4 *__restrict__ x, int n, uint4 *xs) {
+    for (int base = 0; base < n; base += 8 * blockDim.x) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            v[u] = i < n ? __ldg(x + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            if (i < n) xs[i] = v[u];
+        }
+    }
+}
+
+// x: the staged rows (shared memory) or, past kRgStageMax, global memory
 template <int TM>
 __device__ __forceinline__ void router_rows(const uint4 *__restrict__ x, const uint4 *__restrict__ wr, int T, int E,
                                             int H8, float *__restrict__ logits) {
@@ -68,7 +88,7 @@ __device__ __forceinline__ void router_rows(const uint4 *__restrict__ x, const u
                 if (c < H8) {
 #pragma unroll
                     for (int t = 0; t < TM; ++t)
-                        if (t < T) acc[t] += dot8(w[u], __ldg(x + (size_t)t * H8 + c));
+                        if (t < T) acc[t] += dot8(w[u], x[(size_t)t * H8 + c]);
                 }
             }
         }
@@ -97,11 +117,17 @@ struct RouterArgs {
 
 template <int TM>
 __global__ void __launch_bounds__(kRgThreads) router_gemv_kernel(const RouterArgs a) {
-    extern __shared__ int rg_smem[];
+    extern __shared__ uint4 rg_smem4[];
     __shared__ int s_last;
     pdl_wait();
     pdl_trigger();
-    router_rows<TM>(a.x, a.wr, a.T, a.E, a.H8, a.logits);
+    const int nx = a.T * a.H8;
+    const bool staged = (size_t)nx * 16 <= kRgStageMax;
+    if (staged) {
+        stage_x(a.x, nx, rg_smem4);
+        __syncthreads();
+    }
+    router_rows<TM>(staged ? rg_smem4 : a.x, a.wr, a.T, a.E, a.H8, a.logits);
     if (!a.fused) return;
     // release this thread's logits, then take a ticket; the CTA with the
     // last ticket sees every CTA's logits
@@ -113,7 +139,7 @@ __global__ void __launch_bounds__(kRgThreads) router_gemv_kernel(const RouterArg
     __threadfence();
     const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int P = a.T * a.k;
-    int *s_ids = rg_smem;                                        // [P]
+    int *s_ids = reinterpret_cast<int *>(rg_smem4 + (staged ? nx : 0));  // [P], after the staged x rows
     int *s_align = s_ids + ((P + 31) & ~31);                     // align_block scratch
     uint32_t *s_key = reinterpret_cast<uint32_t *>(s_align + align_smem_ints(a.WS, a.E));  // [warps][E]
     for (int t = warp; t < a.T; t += nwarps)
@@ -125,21 +151,33 @@ __global__ void __launch_bounds__(kRgThreads) router_gemv_kernel(const RouterArg
     if (threadIdx.x == 0) a.ctrl[kCtrlRouterTicket] = 0;  // ready for the next call on this workspace
 }
 
-static size_t gemv_smem(int T, int E, int k) {
-    const int P = T * k, WS = align_slices(P);
-    const int rw = T < kRgThreads / 32 ? T : kRgThreads / 32;
-    return (((size_t)(P + 31) & ~(size_t)31) + align_smem_ints(WS, E) + (size_t)rw * E) * sizeof(int);
+// shared memory of a GEMV launch: the staged x rows (when they fit the
+// staging budget), then, for the fused launch, the routing and grouping
+static size_t x_stage_bytes(int T, int H) {
+    const size_t b = (size_t)T * H * 2;
+    return b <= kRgStageMax ? b : 0;
 }
 
-bool router_fusable(int T, int E, int k, size_t smem_limit) {
-    return T >= 1 && T <= kRgMaxT && 32 * align_slices(T * k) <= kRgThreads && gemv_smem(T, E, k) <= smem_limit;
+static size_t gemv_smem(int T, int E, int k, int H, bool fused) {
+    size_t b = x_stage_bytes(T, H);
+    if (fused) {
+        const int P = T * k, WS = align_slices(P);
+        const int rw = T < kRgThreads / 32 ? T : kRgThreads / 32;
+        b += (((size_t)(P + 31) & ~(size_t)31) + align_smem_ints(WS, E) + (size_t)rw * E) * sizeof(int);
+    }
+    return b;
+}
+
+bool router_fusable(int T, int E, int k, int H, size_t smem_limit) {
+    return T >= 1 && T <= kRgMaxT && 32 * align_slices(T * k) <= kRgThreads &&
+           gemv_smem(T, E, k, H, true) <= smem_limit;
 }
 
 static cudaError_t launch_gemv(const RouterArgs &a, int num_sms, cudaStream_t stream) {
     const int wpb = kRgThreads / 32;
     int grid = (a.E + wpb - 1) / wpb;
     if (grid > 4 * num_sms) grid = 4 * num_sms;
-    const size_t smem = a.fused ? gemv_smem(a.T, a.E, a.k) : 0;
+    const size_t smem = gemv_smem(a.T, a.E, a.k, 8 * a.H8, a.fused != 0);
     static int configured[5][128];
 #define MOE_RG(TM, IDX)                                                                          \
     do {                                                                                         \
