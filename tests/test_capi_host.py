@@ -94,6 +94,43 @@ def test_gate_up_and_down_validate_before_launch(lib):
              None) == moe.MOE_ERR_INVALID_ARG                                  # null topk_w
 
 
+def test_new_calls_validate_before_the_device(lib):
+    """Forced-family, NVFP4, router and AWQ-import calls reject malformed
+    arguments on the host (no device is touched: there is none here)."""
+    buf = (ctypes.c_uint8 * 512)()
+    p = ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16
+    need = lib.moe_workspace_bytes(4, 16, 2, 256, 64)
+    # _ex: an unknown family, and the usual checks
+    gu = lambda path, H=256: lib.moe_w4a16_gate_up_silu_ex(p, p, p, p, 32, p, p, p, p, 4, 16, 2, H, 64, p, p,
+                                                          need, path, None)
+    assert gu(7) == moe.MOE_ERR_INVALID_ARG and gu(-1) == moe.MOE_ERR_INVALID_ARG
+    assert gu(moe.MOE_PATH_DECODE, H=250) == moe.MOE_ERR_INVALID_ARG
+    dn = lambda path: lib.moe_w4a16_down_combine_ex(p, p, p, p, 32, p, p, p, p, p, 4, 16, 2, 256, 64, p, p, need,
+                                                    path, None)
+    assert dn(4) == moe.MOE_ERR_INVALID_ARG
+    # NVFP4: null scale pointer, short workspace, bad sizes
+    assert lib.moe_nvfp4_gate_up_silu(p, p, None, p, p, p, p, p, 4, 16, 2, 256, 64, p, p, need,
+                                      None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_nvfp4_down_combine(p, p, p, p, p, p, p, p, p, 4, 16, 2, 256, 64, p, p, need - 256,
+                                      None) == moe.MOE_ERR_WORKSPACE
+    assert lib.moe_nvfp4_moe_layer(p, p, p, p, p, p, p, p, 4, 16, 3, 256, 60, p, p, p, p, 1 << 20,
+                                   None) == moe.MOE_ERR_INVALID_ARG                     # I % 32
+    # router: H % 32, misaligned x, no workspace for the fused call
+    assert lib.moe_router_logits(p, p, 4, 16, 250, p, None, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_logits(p + 2, p, 4, 16, 256, p, None, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_route_align(p, p, 4, 16, 2, 256, p, p, p, p, p, p, p, None, 0,
+                                      None) == moe.MOE_ERR_WORKSPACE
+    assert lib.moe_router_route_align(p, p, 4, 2048, 2, 256, p, p, p, p, p, p, p, p, 512,
+                                      None) == moe.MOE_ERR_UNSUPPORTED                  # E > 1024
+    # AWQ import: misplaced rows, K % 32, group size, overflowing destination
+    imp = lambda E, K, N, g, Nd, r0: lib.moe_awq_import(p, p, p, E, K, N, g, p, p, p, Nd, r0, None)
+    assert imp(1, 64, 16, 32, 32, 4) == moe.MOE_ERR_INVALID_ARG
+    assert imp(1, 48, 16, 32, 32, 0) == moe.MOE_ERR_INVALID_ARG
+    assert imp(1, 64, 16, 128, 32, 0) == moe.MOE_ERR_UNSUPPORTED
+    assert imp(1, 64, 16, 32, 16, 8) == moe.MOE_ERR_INVALID_ARG
+    assert imp(2048, 64, 16, 32, 16, 0) == moe.MOE_ERR_UNSUPPORTED
+
+
 def test_product_path_does_not_import_the_oracle():
     pkg = os.path.dirname(moe.__file__)
     for root, _, files in os.walk(pkg):

@@ -138,6 +138,11 @@ bool all_aligned(const Ps *...ps) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+bool path_value_ok(int path) {
+    return path == MOE_PATH_AUTO || path == MOE_PATH_DECODE || path == MOE_PATH_TENSOR_CORE ||
+           path == MOE_PATH_STREAM;
+}
+
 bool path_supported(int path, int T, int E, int k, int H, int I, size_t smem) {
     switch (path) {
         case MOE_PATH_DECODE: return decode_supported(T, E, k, H, I, smem);
@@ -166,8 +171,7 @@ int nvfp4_path(int T, int E, int k, int H, int I, size_t smem) {
 }
 int resolve_path(int *path, int T, int E, int k, int H, int I, size_t smem) {
     if (*path != MOE_PATH_AUTO) {
-        if (*path != MOE_PATH_DECODE && *path != MOE_PATH_TENSOR_CORE && *path != MOE_PATH_STREAM)
-            return MOE_ERR_INVALID_ARG;
+        if (!path_value_ok(*path)) return MOE_ERR_INVALID_ARG;
         return path_supported(*path, T, E, k, H, I, smem) ? MOE_OK : MOE_ERR_UNSUPPORTED;
     }
     const int tp = tuned_path(T, E, k, H, I);
@@ -295,7 +299,7 @@ MOE_EXPORT int moe_w4a16_gate_up_silu_ex(const uint16_t *x, const uint32_t *w13_
     if (st != MOE_OK) return st;
     if ((st = check_group(group_size)) != MOE_OK) return st;
     if (!all_aligned(x, w13_q, w13_s, w13_z, expert_offsets, sorted_pair, active_experts,
-                     num_active, h))
+                     num_active, h) || !path_value_ok(path))
         return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
         return MOE_ERR_WORKSPACE;
@@ -366,6 +370,7 @@ MOE_EXPORT int moe_w4a16_down_combine_ex(const uint16_t *h, const uint32_t *w2_q
     int st = check_down_combine_args(h, w2_q, w2_s, w2_z, group_size, expert_offsets, sorted_pair,
                                      active_experts, num_active, topk_w, T, E, k, H, I, out);
     if (st != MOE_OK) return st;
+    if (!path_value_ok(path)) return MOE_ERR_INVALID_ARG;
     if (!workspace || !aligned16(workspace) || ws_bytes < moe_workspace_bytes(T, E, k, H, I))
         return MOE_ERR_WORKSPACE;
     if (T == 0) return MOE_OK;
