@@ -168,6 +168,12 @@ __device__ inline void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrival at a named barrier without waiting (the producer side of a
+// producer/consumer hand-off: the consumers bar.sync on the same id).
+__device__ inline void named_barrier_arrive(int id, int threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---------------------------------------------------------------- dependent launch
 // Programmatic dependent launch: every kernel of the library is launched
 // with programmatic stream serialisation, so it can be scheduled while its

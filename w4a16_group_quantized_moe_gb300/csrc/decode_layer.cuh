@@ -56,6 +56,11 @@ constexpr uint32_t kPollTries = 1u << 20;  // bounded wait (about a second) for 
 // Stamps of the optional phase timeline (8 per CTA, global timer, ns).
 enum { kLtEntry = 0, kLtGrouped, kLtFirstIssue, kLtFirstLanded, kLtGateUpDone, kLtDownReady, kLtDownDone, kLtExit };
 
+// Named barriers of the one-token path (0 is __syncthreads): the staging
+// warps' hand-off of the x rows to the router warp, and the staging warps'
+// own barrier.
+enum { kBarXReady = 1, kBarStagers = 2 };
+
 struct LayerArgs {
     const float *logits;  // [T][E]
     const __half *x;      // [T][H]
@@ -257,78 +262,128 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     pdl_wait();
     pdl_trigger();
 
-    // ---- 1. route (warps < T) while the other warps stage the x rows
-    if (warp < a.T) {
-        const bool lead = cta == 0;
-        const float *row = a.logits + (size_t)warp * a.E;
-        int32_t *ids = lead ? a.topk_ids : nullptr;
-        float *w = lead ? a.topk_w : nullptr;
-        // keys in this warp's task ring, which no copy has touched yet
-        route_token_compact(row, a.E, k, warp, ids, w, s_ids, s_w, reinterpret_cast<uint32_t *>(ring));
-    } else if (NTH > 32 * a.T) {  // the host keeps NW > T
-        dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
-    }
-    __syncthreads();
-
-    // ---- group the pairs: rank of pair p = #(expert < e) + #(earlier pairs of e)
-    for (int p = tid; p < P; p += NTH) {
-        const int e = s_ids[p];
-        int less = 0, same = 0, before = 0;
-        for (int q = 0; q < P; ++q) {
-            const int f = s_ids[q];
-            less += f < e;
-            same += f == e;
-            before += (f == e) & (q < p);
-        }
-        s_pairs[less + before] = p;
-        s_tok[less + before] = p / k;
-        g_less[p] = less;
-        g_same[p] = same;
-        g_first[p] = before == 0;
-        if (before == 0) atomicAdd(const_cast<int *>(&s_misc[0]), 1);
-    }
-    __syncthreads();
-    for (int p = tid; p < P; p += NTH) {
-        if (!g_first[p]) continue;
-        const int e = s_ids[p];
-        int slot = 0;
-        for (int q = 0; q < P; ++q) slot += g_first[q] & (s_ids[q] < e);
-        s_act[slot] = e;
-        s_lo[slot] = g_less[p];
-        s_hi[slot] = g_less[p] + g_same[p];
-    }
-    __syncthreads();
-
-    if (tid == 0 && tl) {
-        tl[cta * 8 + kLtEntry] = t_entry;
-        stamp(kLtGrouped);
-    }
-
-    // ---- 2. this CTA's shares of both task lists (weighted, contiguous)
-    const int A = s_misc[0];
+    // One token: each selected expert has exactly one row, so the segments
+    // can be kept in rank order (segment j = rank j, pair j) and every
+    // CTA's task shares follow from k alone.  The routing warp publishes each
+    // rank as its round decides it; the other warps compute their shares
+    // meanwhile and issue each task's copies as soon as its expert is
+    // ranked.  Results are those of the general path (h, y and the combine
+    // are indexed by pair, the segment order is internal).
+    const bool one = a.T == 1;
+    volatile int *s_ranked = s_misc + 1;  // ranks published so far (one-token path)
+    int A, b1, e1, b2, e2;
     const int TPE1 = (I + RT1 - 1) / RT1, TPE2 = (H + RT2 - 1) / RT2;
-    {
-        const long long W1 = (long long)TPE1 * (2 * A + P), W2 = (long long)TPE2 * (2 * A + P);
-        if (tid == 0) {
-            s_misc[4] = 0; s_misc[5] = A * TPE1; s_misc[6] = 0; s_misc[7] = A * TPE2;
+    if (one) {
+        A = k;
+        __syncthreads();  // the zeroed counter is visible before anyone polls it
+        if (warp == 0) {
+            if (lane < k) {
+                s_lo[lane] = lane;
+                s_hi[lane] = lane + 1;
+                s_pairs[lane] = lane;
+                s_tok[lane] = 0;
+            }
+            const bool lead = cta == 0;
+            route_token_compact(a.logits, a.E, k, 0, lead ? a.topk_ids : nullptr, lead ? a.topk_w : nullptr, s_ids,
+                                s_w, reinterpret_cast<uint32_t *>(ring), s_act, s_ranked);
+            if (tid == 0) s_misc[0] = k;
+        } else {
+            dec_stage_rows(a.x, 1, H, G1, cache, tid - 32, NTH - 32);
+            named_barrier_arrive(kBarXReady, NTH);   // the router warp syncs on it later
+            named_barrier(kBarStagers, NTH - 32);    // x visible to every staging warp
+        }
+        // shares: A = P = k, every task of expert a weighs 3, expert a's tasks
+        // start at weight 3 a tpe (the closed form of share_start)
+        auto share1 = [&](long long w, int tpe) {
+            const long long a3 = 3LL * tpe;
+            const int ax = (int)(w / a3);
+            return ax * tpe + (int)((w - ax * a3 + 2) / 3);
+        };
+        const long long W1 = 3LL * TPE1 * k, W2 = 3LL * TPE2 * k;
+        b1 = share1(W1 * cta / NC, TPE1);
+        e1 = cta + 1 < NC ? share1(W1 * (cta + 1) / NC, TPE1) : k * TPE1;
+        b2 = share1(W2 * cta / NC, TPE2);
+        e2 = cta + 1 < NC ? share1(W2 * (cta + 1) / NC, TPE2) : k * TPE2;
+        if (tid == 0 && tl) {
+            tl[cta * 8 + kLtEntry] = t_entry;
+            stamp(kLtGrouped);
+        }
+    } else {
+        // ---- 1. route (warps < T) while the other warps stage the x rows
+        if (warp < a.T) {
+            const bool lead = cta == 0;
+            const float *row = a.logits + (size_t)warp * a.E;
+            int32_t *ids = lead ? a.topk_ids : nullptr;
+            float *w = lead ? a.topk_w : nullptr;
+            // keys in this warp's task ring, which no copy has touched yet
+            route_token_compact(row, a.E, k, warp, ids, w, s_ids, s_w, reinterpret_cast<uint32_t *>(ring));
+        } else if (NTH > 32 * a.T) {  // the host keeps NW > T
+            dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
         }
         __syncthreads();
-        int *sm = const_cast<int *>(s_misc);
-        share_start(W1 * cta / NC, A, TPE1, s_lo, s_hi, sm + 4, tid, NTH);
-        if (cta + 1 < NC) share_start(W1 * (cta + 1) / NC, A, TPE1, s_lo, s_hi, sm + 5, tid, NTH);
-        share_start(W2 * cta / NC, A, TPE2, s_lo, s_hi, sm + 6, tid, NTH);
-        if (cta + 1 < NC) share_start(W2 * (cta + 1) / NC, A, TPE2, s_lo, s_hi, sm + 7, tid, NTH);
+
+        // ---- group the pairs: rank of pair p = #(expert < e) + #(earlier pairs of e)
+        for (int p = tid; p < P; p += NTH) {
+            const int e = s_ids[p];
+            int less = 0, same = 0, before = 0;
+            for (int q = 0; q < P; ++q) {
+                const int f = s_ids[q];
+                less += f < e;
+                same += f == e;
+                before += (f == e) & (q < p);
+            }
+            s_pairs[less + before] = p;
+            s_tok[less + before] = p / k;
+            g_less[p] = less;
+            g_same[p] = same;
+            g_first[p] = before == 0;
+            if (before == 0) atomicAdd(const_cast<int *>(&s_misc[0]), 1);
+        }
         __syncthreads();
+        for (int p = tid; p < P; p += NTH) {
+            if (!g_first[p]) continue;
+            const int e = s_ids[p];
+            int slot = 0;
+            for (int q = 0; q < P; ++q) slot += g_first[q] & (s_ids[q] < e);
+            s_act[slot] = e;
+            s_lo[slot] = g_less[p];
+            s_hi[slot] = g_less[p] + g_same[p];
+        }
+        __syncthreads();
+
+        if (tid == 0 && tl) {
+            tl[cta * 8 + kLtEntry] = t_entry;
+            stamp(kLtGrouped);
+        }
+
+        // ---- 2. this CTA's shares of both task lists (weighted, contiguous)
+        A = s_misc[0];
+        {
+            const long long W1 = (long long)TPE1 * (2 * A + P), W2 = (long long)TPE2 * (2 * A + P);
+            if (tid == 0) {
+                s_misc[4] = 0; s_misc[5] = A * TPE1; s_misc[6] = 0; s_misc[7] = A * TPE2;
+            }
+            __syncthreads();
+            int *sm = const_cast<int *>(s_misc);
+            share_start(W1 * cta / NC, A, TPE1, s_lo, s_hi, sm + 4, tid, NTH);
+            if (cta + 1 < NC) share_start(W1 * (cta + 1) / NC, A, TPE1, s_lo, s_hi, sm + 5, tid, NTH);
+            share_start(W2 * cta / NC, A, TPE2, s_lo, s_hi, sm + 6, tid, NTH);
+            if (cta + 1 < NC) share_start(W2 * (cta + 1) / NC, A, TPE2, s_lo, s_hi, sm + 7, tid, NTH);
+            __syncthreads();
+        }
+        b1 = s_misc[4]; e1 = s_misc[5]; b2 = s_misc[6]; e2 = s_misc[7];
     }
-    const int b1 = s_misc[4], e1 = s_misc[5], b2 = s_misc[6], e2 = s_misc[7];
-    // this warp's tasks: b1 + warp + i*NW (i < n1), then b2 + warp + j*NW
-    const int n1 = e1 - b1 > warp ? (e1 - b1 - warp + NW - 1) / NW : 0;
+    // this warp's tasks: b1 + gw + i*gNW (i < n1), then b2 + warp + j*NW; with
+    // one token the routing warp takes no gate/up task (gw = warp - 1 over the
+    // other NW - 1 warps), so no task waits for the router to finish
+    const int gw = one ? warp - 1 : warp, gNW = one ? NW - 1 : NW;
+    const int n1 = (gw >= 0 && e1 - b1 > gw) ? (e1 - b1 - gw + gNW - 1) / gNW : 0;
     const int n2 = e2 - b2 > warp ? (e2 - b2 - warp + NW - 1) / NW : 0;
     const int ntask = n1 + n2;
 
     // positions of the next task to issue and of the two tasks in the slots
     int iss = 0;
-    TaskPos ip{(b1 + warp) / TPE1, (b1 + warp) % TPE1};
+    TaskPos ip{gw >= 0 ? (b1 + gw) / TPE1 : 0, gw >= 0 ? (b1 + gw) % TPE1 : 0};
     if (n1 == 0) ip = TaskPos{(b2 + warp) / TPE2, (b2 + warp) % TPE2};
     TaskPos q0{0, 0}, q1{0, 0};  // tasks in flight, oldest first
 
@@ -344,7 +399,19 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     // fetch task `iss` (position ip) into slot iss % 2, then advance ip.
     // Lane 0 posts the expected bytes; lanes 0-5 (gate/up: codes, scales,
     // zeros of gate and up) or 0-2 (down) then issue one bulk copy each.
+    bool dead = false;
     auto issue = [&]() {
+        if (one) {
+            // one token: this task's expert may still be being ranked
+            uint32_t it = 0;
+            while (*s_ranked <= ip.ai && ++it < polls) __nanosleep(32);
+            __threadfence_block();
+            if (!__all_sync(0xffffffffu, it < polls)) {
+                if (lane == 0) set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
+                dead = true;
+                return;
+            }
+        }
         const bool gate = iss < n1;
         Cursor cu;
         make_cursor(ip, gate, cu);
@@ -384,12 +451,13 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         if (iss == 0) q0 = ip; else q1 = ip;
         ++iss;
         if (iss == n1) ip = TaskPos{(b2 + warp) / TPE2, (b2 + warp) % TPE2};
-        else task_advance(ip, NW, iss < n1 ? TPE1 : TPE2);
+        else task_advance(ip, iss < n1 ? gNW : NW, iss < n1 ? TPE1 : TPE2);
     };
 
     const int nfirst = ntask < kLayerSlots ? ntask : kLayerSlots;
-    for (int i = 0; i < nfirst; ++i) issue();
+    for (int i = 0; i < nfirst && !dead; ++i) issue();
     if (tid == 0) stamp(kLtFirstIssue);
+    if (one && warp == 0) named_barrier(kBarXReady, NTH);  // the router computes after x is staged
     int consumed = 0;
 
     const TaskDims td1{2 * I, H, I, P, k}, td2{H, I, H, P, k};
@@ -398,7 +466,6 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     for (int b = 0; b < 2; ++b)
 #pragma unroll
         for (int t = 0; t < kDecPass; ++t) acc1[0][b][t] = acc2[b][0][t] = 0.f;
-    bool dead = false;
     int hrow0 = 0;
 
     for (int i = 0; i <= ntask; ++i) {
@@ -512,7 +579,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             }
         }
         __syncwarp();
-        if (iss < ntask) issue();
+        if (iss < ntask && !dead) issue();
     }
     // never leave with a copy in flight into this CTA's shared memory
     for (int j = consumed; j < iss; ++j)

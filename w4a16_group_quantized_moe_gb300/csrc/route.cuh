@@ -104,12 +104,16 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
 // rounds scans the lane's keys in ascending expert order (first maximum =
 // lowest index), takes the warp maximum and, among lanes holding it, the
 // lowest expert index; the winner's key is cleared.  Results are identical
-// to route_token's.  E <= 1024.
+// to route_token's.  E <= 1024.  With pub_n, every round also publishes its
+// winner at once: pub_id[s] = expert of rank s, then (after a block-scope
+// fence) *pub_n = s + 1, so other warps of the CTA can act on the first
+// ranks while the later ones are still being chosen.
 template <bool FRESH = false>
 __device__ __forceinline__ void route_token_compact(const float *__restrict__ row, int E, int k, int t,
                                                     int32_t *__restrict__ topk_ids,
                                                     float *__restrict__ topk_w, int *s_ids, float *s_w,
-                                                    uint32_t *s_key) {
+                                                    uint32_t *s_key, int *pub_id = nullptr,
+                                                    volatile int *pub_n = nullptr) {
     const int lane = threadIdx.x & 31;
     {
         // every load first (one memory round trip), then the keys
@@ -139,6 +143,11 @@ __device__ __forceinline__ void route_token_compact(const float *__restrict__ ro
         const int win = (int)__reduce_min_sync(0xffffffffu, b0 == kmax ? (uint32_t)e0 : 0xffffffffu);
         if (lane == s) my_id = win;
         if (lane == (win & 31)) s_key[win] = 0u;
+        if (pub_n && lane == 0) {
+            pub_id[s] = win;
+            __threadfence_block();
+            *pub_n = s + 1;
+        }
         __syncwarp();
     }
     const float my_logit = lane < k ? load_logit<FRESH>(row + my_id) : 0.f;
