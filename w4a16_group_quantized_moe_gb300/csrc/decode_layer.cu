@@ -5,6 +5,11 @@
 namespace moe {
 
 // ---------------------------------------------------------------- host side
+#ifndef PAIR_SEGMENTS_MAX_T
+#define PAIR_SEGMENTS_MAX_T 4
+#endif
+constexpr int kPairSegmentsMaxT = PAIR_SEGMENTS_MAX_T;  // on the Qwen4Exp geometry
+
 namespace {
 
 // Lanes per gate/up row pair and per down row: about five groups per lane,
@@ -45,6 +50,24 @@ LayerPlan layer_plan(int T, int E, int k, int H, int I, int num_sms, size_t smem
 
 }  // namespace
 
+// One-row segment per pair (see decode_layer_kernel): with one token it is
+// the grouping itself; above, it streams an expert once per token that chose
+// it, traded against starting every copy as soon as its pair is ranked.
+// Measured on GB300 (one-call layer, mean us, grouped / pair segments):
+//   Qwen4Exp (2560, 640, 512, 10): T=1 27.3 / 25.1, T=2 34.9 / 35.0,
+//       T=4 52.3 / 49.3, T=8 82.0 / 106.5
+//   TP4 shard (2560, 160, 512, 10, hot experts): T=2 25.0 / 22.3,
+//       T=4 32.1 / 26.0, T=8 41.6 / 41.0
+// Compiled for H = 2560 with I = 640 or 160 (the instantiations with a
+// compile-time group count); other shapes take the grouped path.
+int pair_segments(int T, int E, int k, int H, int I) {
+    (void)E; (void)k;
+    if (H != 2560) return 0;
+    if (I == 640) return T <= kPairSegmentsMaxT ? 1 : 0;
+    if (I == 160) return T <= 8 ? 1 : 0;
+    return 0;
+}
+
 bool layer_fusable(int T, int E, int k, int H, int I, int num_sms, size_t smem_limit) {
     return layer_plan(T, E, k, H, I, num_sms, smem_limit).ok;
 }
@@ -65,6 +88,7 @@ static cudaError_t launch_decode_layer_f(const float *logits, const __half *x, c
     a.topk_ids = topk_ids; a.topk_w = topk_w; a.out = out;
     a.h = h; a.y = y; a.blkctr = blkctr; a.done = done; a.exitctr = exitctr; a.err = err;
     a.nw = pl.nw; a.hrows = pl.hrows; a.slot_bytes = pl.slot_bytes;
+    a.pair_mode = pair_segments(T, E, k, H, I);
     const int G1 = H / 32, G2 = I / 32;
     // the geometries the layer is specified on get compile-time group counts
     if (G1 == 80 && pl.L1 == 16 && G2 == 20 && pl.L2 == 4)

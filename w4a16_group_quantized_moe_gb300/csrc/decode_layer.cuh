@@ -56,8 +56,8 @@ constexpr uint32_t kPollTries = 1u << 20;  // bounded wait (about a second) for 
 // Stamps of the optional phase timeline (8 per CTA, global timer, ns).
 enum { kLtEntry = 0, kLtGrouped, kLtFirstIssue, kLtFirstLanded, kLtGateUpDone, kLtDownReady, kLtDownDone, kLtExit };
 
-// Named barriers of the one-token path (0 is __syncthreads): the staging
-// warps' hand-off of the x rows to the router warp, and the staging warps'
+// Named barriers of the pair-segment path (0 is __syncthreads): the staging
+// warps' hand-off of the x rows to the routing warps, and the staging warps'
 // own barrier.
 enum { kBarXReady = 1, kBarStagers = 2 };
 
@@ -83,6 +83,7 @@ struct LayerArgs {
     int nw;               // warps per CTA
     int hrows;            // h rows the shared cache holds
     uint32_t slot_bytes;  // one task buffer
+    int pair_mode;        // 1: one-row segment per pair, in pair order (see the kernel)
 };
 
 // Shared memory: meta ints (ids, weights, sorted pairs, active experts,
@@ -211,7 +212,7 @@ __device__ __forceinline__ void share_start(long long w, int A, int tpe, const i
     }
 }
 
-template <int L1, int GT1, int L2, int GT2, int FMT>
+template <int L1, int GT1, int L2, int GT2, int FMT, bool PAIRS>
 __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(const LayerArgs a) {
     using T1 = DecTraits<kDecGateUp, L1, 1>;
     using T2 = DecTraits<kDecDown, L2, 2>;
@@ -262,48 +263,52 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     pdl_wait();
     pdl_trigger();
 
-    // One token: each selected expert has exactly one row, so the segments
-    // can be kept in rank order (segment j = rank j, pair j) and every
-    // CTA's task shares follow from k alone.  The routing warp publishes each
-    // rank as its round decides it; the other warps compute their shares
-    // meanwhile and issue each task's copies as soon as its expert is
-    // ranked.  Results are those of the general path (h, y and the combine
-    // are indexed by pair, the segment order is internal).
-    const bool one = a.T == 1;
-    volatile int *s_ranked = s_misc + 1;  // ranks published so far (one-token path)
+    // Pair segments (a.pair_mode; always with one token, where it changes
+    // nothing else): every pair p = t*k + j is its own one-row segment, in
+    // pair order, even when two tokens chose the same expert (that expert's
+    // weights are then streamed once per pair).  Every CTA's task shares then
+    // follow from P alone, each routing warp publishes its token's ranks as
+    // its rounds decide them, and the other warps compute their shares
+    // meanwhile and issue each task's copies as soon as its pair is ranked.
+    // h, y and the combine are indexed by pair, so the arithmetic per pair is
+    // that of the grouped path.
+    constexpr bool one = PAIRS;  // a separate instantiation: the grouped path carries none of it
+    volatile int *s_ranked = g_less;  // [T] ranks published per token (pair segments)
     int A, b1, e1, b2, e2;
     const int TPE1 = (I + RT1 - 1) / RT1, TPE2 = (H + RT2 - 1) / RT2;
     if (one) {
-        A = k;
-        __syncthreads();  // the zeroed counter is visible before anyone polls it
-        if (warp == 0) {
+        A = P;
+        for (int t = tid; t < a.T; t += NTH) s_ranked[t] = 0;
+        __syncthreads();  // the zeroed counters are visible before anyone polls them
+        if (warp < a.T) {
             if (lane < k) {
-                s_lo[lane] = lane;
-                s_hi[lane] = lane + 1;
-                s_pairs[lane] = lane;
-                s_tok[lane] = 0;
+                const int p = warp * k + lane;
+                s_lo[p] = p;
+                s_hi[p] = p + 1;
+                s_pairs[p] = p;
+                s_tok[p] = warp;
             }
             const bool lead = cta == 0;
-            route_token_compact(a.logits, a.E, k, 0, lead ? a.topk_ids : nullptr, lead ? a.topk_w : nullptr, s_ids,
-                                s_w, reinterpret_cast<uint32_t *>(ring), s_act, s_ranked);
-            if (tid == 0) s_misc[0] = k;
+            route_token_compact(a.logits + (size_t)warp * a.E, a.E, k, warp, lead ? a.topk_ids : nullptr,
+                                lead ? a.topk_w : nullptr, s_ids, s_w, reinterpret_cast<uint32_t *>(ring),
+                                s_act + warp * k, s_ranked + warp);
         } else {
-            dec_stage_rows(a.x, 1, H, G1, cache, tid - 32, NTH - 32);
-            named_barrier_arrive(kBarXReady, NTH);   // the router warp syncs on it later
-            named_barrier(kBarStagers, NTH - 32);    // x visible to every staging warp
+            dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
+            named_barrier_arrive(kBarXReady, NTH);        // the routing warps sync on it later
+            named_barrier(kBarStagers, NTH - 32 * a.T);   // x visible to every staging warp
         }
-        // shares: A = P = k, every task of expert a weighs 3, expert a's tasks
-        // start at weight 3 a tpe (the closed form of share_start)
+        // shares: A = P one-row segments, every task weighs 3, segment p's
+        // tasks start at weight 3 p tpe (the closed form of share_start)
         auto share1 = [&](long long w, int tpe) {
             const long long a3 = 3LL * tpe;
             const int ax = (int)(w / a3);
             return ax * tpe + (int)((w - ax * a3 + 2) / 3);
         };
-        const long long W1 = 3LL * TPE1 * k, W2 = 3LL * TPE2 * k;
+        const long long W1 = 3LL * TPE1 * P, W2 = 3LL * TPE2 * P;
         b1 = share1(W1 * cta / NC, TPE1);
-        e1 = cta + 1 < NC ? share1(W1 * (cta + 1) / NC, TPE1) : k * TPE1;
+        e1 = cta + 1 < NC ? share1(W1 * (cta + 1) / NC, TPE1) : P * TPE1;
         b2 = share1(W2 * cta / NC, TPE2);
-        e2 = cta + 1 < NC ? share1(W2 * (cta + 1) / NC, TPE2) : k * TPE2;
+        e2 = cta + 1 < NC ? share1(W2 * (cta + 1) / NC, TPE2) : P * TPE2;
         if (tid == 0 && tl) {
             tl[cta * 8 + kLtEntry] = t_entry;
             stamp(kLtGrouped);
@@ -374,9 +379,9 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         b1 = s_misc[4]; e1 = s_misc[5]; b2 = s_misc[6]; e2 = s_misc[7];
     }
     // this warp's tasks: b1 + gw + i*gNW (i < n1), then b2 + warp + j*NW; with
-    // one token the routing warp takes no gate/up task (gw = warp - 1 over the
-    // other NW - 1 warps), so no task waits for the router to finish
-    const int gw = one ? warp - 1 : warp, gNW = one ? NW - 1 : NW;
+    // pair segments the routing warps take no gate/up task (gw = warp - T
+    // over the other NW - T warps), so no task waits for a router to finish
+    const int gw = one ? warp - a.T : warp, gNW = one ? NW - a.T : NW;
     const int n1 = (gw >= 0 && e1 - b1 > gw) ? (e1 - b1 - gw + gNW - 1) / gNW : 0;
     const int n2 = e2 - b2 > warp ? (e2 - b2 - warp + NW - 1) / NW : 0;
     const int ntask = n1 + n2;
@@ -402,9 +407,10 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     bool dead = false;
     auto issue = [&]() {
         if (one) {
-            // one token: this task's expert may still be being ranked
+            // pair segments: this task's pair may still be being ranked
+            const int pt = ip.ai / k, pj = ip.ai - pt * k;
             uint32_t it = 0;
-            while (*s_ranked <= ip.ai && ++it < polls) __nanosleep(32);
+            while (s_ranked[pt] <= pj && ++it < polls) __nanosleep(32);
             __threadfence_block();
             if (!__all_sync(0xffffffffu, it < polls)) {
                 if (lane == 0) set_error(a.err, MOE_DEVERR_WAIT_TIMEOUT);
@@ -455,9 +461,9 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     };
 
     const int nfirst = ntask < kLayerSlots ? ntask : kLayerSlots;
-    for (int i = 0; i < nfirst && !dead; ++i) issue();
+    for (int i = 0; i < nfirst && !(one && dead); ++i) issue();
     if (tid == 0) stamp(kLtFirstIssue);
-    if (one && warp == 0) named_barrier(kBarXReady, NTH);  // the router computes after x is staged
+    if (one && warp < a.T) named_barrier(kBarXReady, NTH);  // routers compute after x is staged
     int consumed = 0;
 
     const TaskDims td1{2 * I, H, I, P, k}, td2{H, I, H, P, k};
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             }
         }
         __syncwarp();
-        if (iss < ntask && !dead) issue();
+        if (iss < ntask) issue();  // a warp that found a wait timed out left the loop above
     }
     // never leave with a copy in flight into this CTA's shared memory
     for (int j = consumed; j < iss; ++j)
@@ -652,10 +658,9 @@ struct LayerPlan {
 };
 
 // Cooperative launch of one instantiation: one CTA per SM, all resident.
-template <int L1, int GT1, int L2, int GT2, int FMT>
-cudaError_t launch_layer_t(const LayerArgs &a, const LayerPlan &pl, int num_sms, cudaStream_t stream) {
-    auto kern = decode_layer_kernel<L1, GT1, L2, GT2, FMT>;
-    static int configured[128];
+template <typename K>
+cudaError_t launch_layer_k(K kern, int *configured, const LayerArgs &a, const LayerPlan &pl, int num_sms,
+                           cudaStream_t stream) {
     cudaError_t e = ensure_smem(kern, configured, pl.smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
@@ -673,6 +678,21 @@ cudaError_t launch_layer_t(const LayerArgs &a, const LayerPlan &pl, int num_sms,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Pair segments (a.pair_mode) are compiled for the geometries with a
+// compile-time group count only; elsewhere the grouped path runs.
+template <int L1, int GT1, int L2, int GT2, int FMT>
+cudaError_t launch_layer_t(const LayerArgs &a, const LayerPlan &pl, int num_sms, cudaStream_t stream) {
+    if constexpr (GT1 != 0) {
+        if (a.pair_mode) {
+            static int configured_p[128];
+            return launch_layer_k(decode_layer_kernel<L1, GT1, L2, GT2, FMT, true>, configured_p, a, pl, num_sms,
+                                  stream);
+        }
+    }
+    static int configured[128];
+    return launch_layer_k(decode_layer_kernel<L1, GT1, L2, GT2, FMT, false>, configured, a, pl, num_sms, stream);
 }
 
 #define MOE_LAYER_INSTANCES(X) \
