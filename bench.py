@@ -6,13 +6,16 @@ entry point moe_w4a16_moe_layer (one cooperative launch for decode batches).
 Default workload: Qwen4Exp-geometry decode, 1 token (hidden 2560,
 intermediate 640, 512 experts, top-10, W4A16 g32).
 
-Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA
-events on the launching stream.  Inputs larger than L2: the layer's weights
-exist in NL distinct copies used in turn (a stack of MoE layers), so every
-step reads its active weights from HBM; the router logits rotate over 32
-pre-generated sets so the active experts change from step to step.  Also
-reported: the same step with L2 flushed (a 1 GiB read) before every step,
-which also evicts the kernel's code, and the four step calls.
+Timing: W untimed warm-up steps, then K timed steps issued back to back on
+the launching stream, one pair of CUDA events around all K (each launch
+overlaps the end of the previous step, as in a stack of layers).  Inputs
+larger than L2: the layer's weights exist in NL distinct copies used in
+turn (a stack of MoE layers), so every step reads its active weights from
+HBM; copy i reads its own router-logit and activation set i, so the active
+experts change from step to step.  Also reported: each call timed alone
+(its own events after a GPU sleep, so its launch latency is inside them),
+the same with L2 flushed (a 1 GiB read) before every step, which also
+evicts the kernel's code, and the four step calls.
 
 Multi-GPU: the layer has no cross-token exchange, so N GPUs run N independent
 replicas (weak scaling); value = all ranks' tokens / max-over-ranks time.
@@ -304,7 +307,8 @@ def bench_config(wl, world: int, sets: int) -> dict:
             "l2": f"inputs larger than L2: {NL} distinct copies of the layer's weights "
                   f"({NL * (b['w13'] + b['w2']) * sh.E / 1e9:.1f} GB) used in turn, so the {NL - 1} steps "
                   f"between two uses of a copy stream >= {(NL - 1) * per_step / 1e6:.0f} MB of other "
-                  f"weights through the 126 MB L2; router logits rotate over {sets} sets"}
+                  f"weights through the 126 MB L2; copy i reads router-logit and activation set i; "
+                  f"the K timed steps run back to back"}
 
 
 def run_reference(args, wl):
@@ -400,6 +404,14 @@ class LayerRig:
         self.logits_buf = torch.empty((sh.T, sh.E), dtype=torch.float32, device=dev)
         self.x_buf = torch.empty((sh.T, sh.H), dtype=torch.float16, device=dev)
         self.stream = torch.cuda.current_stream(dev)
+        # back-to-back steps: weight copy i reads its own input buffers, which
+        # hold input set i (staged before the timed region)
+        self.b2b_in, self.b2b_calls = [], []
+        for ly in self.layers:
+            lb, xb = torch.empty_like(self.logits_buf), torch.empty_like(self.x_buf)
+            ly.bind(lb, xb, self.stream)
+            self.b2b_in.append((lb, xb))
+            self.b2b_calls.append(ly.layer_call)
         self.steps4 = [ly.bind(self.logits_buf, self.x_buf, self.stream) for ly in self.layers]
         self.calls = [ly.layer_call for ly in self.layers]
         # active experts of every set (for the algorithmic bytes)
@@ -441,6 +453,30 @@ class LayerRig:
             ev[j][1].record(self.stream)
         torch.cuda.synchronize()
         return np.array([e[0].elapsed_time(e[1]) for e in ev])
+
+    def timed_b2b(self, n, first):
+        """Milliseconds of n layer calls issued back to back (step s runs on
+        weight copy s % NL with input set s % NL), one event pair around all
+        of them: each launch overlaps the end of the previous step, as in a
+        stack of layers."""
+        import torch
+        for i, (lb, xb) in enumerate(self.b2b_in):
+            lg, xx = self.sets[i % len(self.sets)]
+            lb.copy_(lg)
+            xb.copy_(xx)
+        # ~1 ms of GPU work ahead of the events: the host enqueues the calls
+        # faster than the GPU runs them, so no host gap falls inside
+        torch.cuda._sleep(2000000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for j in range(n):
+            self.b2b_calls[(first + j) % self.NL]()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return float(e0.elapsed_time(e1))
+
+    def A_b2b(self, first, n):
+        return np.array([self.A_of[((first + s) % self.NL) % len(self.sets)] for s in range(n)])
 
     def check_errors(self, when):
         for ly in self.layers:
@@ -486,14 +522,19 @@ def per_config_figures(moe, dev, geoms, names, sets: int, fmt: str = "w4a16"):
         rig = LayerRig(moe, wl, copies, dev, min(sets, 8), copies_needed(wl, fmt), fmt)
         warm, steps = (3, 30) if big else (20, 400)
         rig.timed(warm, 0, rig.one_call)
+        rig.timed_b2b(warm, 0)
         rig.check_errors(f"during warm-up of {name}")
-        ms = rig.timed(steps, warm, rig.one_call)
+        iso = rig.timed(steps, warm, rig.one_call)
+        tot = rig.timed_b2b(steps, warm)
         rig.check_errors(f"during {name}")
-        A = rig.A_steps(warm, steps)
+        ms = np.full(steps, tot / steps)
+        A = rig.A_b2b(warm, steps)
         roof = roofline_entry(wl, ms, A, fmt)
         out.append({"workload": name, "steps": steps, "warmup": warm,
-                    "layer_us_median": float(np.median(ms) * 1e3), "layer_us_mean": float(ms.mean() * 1e3),
-                    "tokens_per_s": wl.shape.T * steps / (ms.sum() / 1e3),
+                    "layer_us_mean": tot / steps * 1e3,
+                    "layer_us_isolated_median": float(np.median(iso) * 1e3),
+                    "layer_us_isolated_mean": float(iso.mean() * 1e3),
+                    "tokens_per_s": wl.shape.T * steps / (tot / 1e3),
                     "mean_active_experts": float(A.mean()),
                     "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "frac")},
                     "gpu_launches_per_step": layer_launches(moe, *(getattr(wl.shape, f) for f in "TEkHI"))})
@@ -764,20 +805,25 @@ def main():
     with Clocks(local) as clk:
         # the sampler runs across warm-up, the timed steps and the secondary
         # figures, so that it sees the GPU under this load for several periods
-        rig.timed(args.warmup, 0, rig.one_call)
+        rig.timed(min(args.warmup, 50), 0, rig.one_call)
         rig.timed(min(args.warmup, 50), 0, rig.four_calls)
+        rig.timed_b2b(args.warmup, 0)
         rig.check_errors("during warm-up")
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        layer_ms = rig.timed(args.steps, args.warmup, rig.one_call)
+        # the timed region: K layer calls back to back
+        tot_ms_rank = rig.timed_b2b(args.steps, args.warmup)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         rig.check_errors("during timed steps")
-        A_steps = rig.A_steps(args.warmup, args.steps)
-        # secondary figures: the four step calls, and one call with L2 flushed
+        A_steps = rig.A_b2b(args.warmup, args.steps)
+        # secondary figures: each call alone (a ~100 us GPU sleep ahead of
+        # it, so its launch latency is inside its events), the four step
+        # calls, and one call with L2 flushed
         n2 = max(200, min(args.steps, 2000))
+        iso_ms = rig.timed(n2, args.warmup, rig.one_call)
         four_ms = rig.timed(n2, 0, rig.four_calls)
         flushed_ms = rig.timed(n2, 0, rig.one_call, flush=flush_l2)
 
@@ -819,8 +865,9 @@ def main():
             around = around_layer_figures(moe, dev)
     geo_cache.clear()
 
-    tot_ms = max_over_ranks(float(layer_ms.sum()), dev)
+    tot_ms = max_over_ranks(tot_ms_rank, dev)
     value = whole_job_rate(world, T, args.steps, tot_ms)
+    layer_ms = np.full(args.steps, tot_ms / args.steps)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -848,8 +895,10 @@ def main():
             "config": bench_config(wl, world, args.sets),
             "mean_active_experts": float(A_steps.mean()),
             "layer_hbm_gbs": roof["achieved"] if roof["bound"] == "hbm" else None,
-            "layer_us": {"median": med(layer_ms), "p10": float(np.percentile(layer_ms, 10) * 1e3),
-                         "p90": float(np.percentile(layer_ms, 90) * 1e3)},
+            "layer_us": tot_ms / args.steps * 1e3,
+            "layer_us_isolated": {"median": med(iso_ms), "mean": float(iso_ms.mean() * 1e3),
+                                  "p10": float(np.percentile(iso_ms, 10) * 1e3),
+                                  "p90": float(np.percentile(iso_ms, 90) * 1e3), "steps": len(iso_ms)},
             "layer_us_l2_flushed_each_step": med(flushed_ms),
             "layer_us_four_step_calls": med(four_ms),
             "roofline": roof,

@@ -103,7 +103,7 @@ __host__ __device__ inline LayerLayout layer_layout(int T, int H, int I, int P, 
     const size_t xc = (size_t)T * H * 2, hc = (size_t)hrows * I * 2;
     L.ring = L.cache + (uint32_t)align_up(xc > hc ? xc : hc, 128);
     L.bars = L.ring + (uint32_t)nw * kLayerSlots * slot_bytes;
-    L.total = L.bars + (uint32_t)nw * kLayerSlots * 8;
+    L.total = L.bars + (uint32_t)(nw * kLayerSlots + kLayerMaxT) * 8;  // + one per routing warp
     return L;
 }
 
@@ -240,6 +240,8 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *ring = smem + Ly.ring + (size_t)warp * kLayerSlots * a.slot_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * kLayerSlots;
+    // the routing warp's logits copy (warps < T)
+    uint64_t *lbar = reinterpret_cast<uint64_t *>(smem + Ly.bars) + NW * kLayerSlots + (warp & (kLayerMaxT - 1));
     const WarpGeom wg1 = warp_geom(RT1, 2, H), wg2 = warp_geom(RT2, 1, I);
     const int cta = blockIdx.x, NC = gridDim.x;
 
@@ -291,7 +293,7 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             const bool lead = cta == 0;
             route_token_compact(a.logits + (size_t)warp * a.E, a.E, k, warp, lead ? a.topk_ids : nullptr,
                                 lead ? a.topk_w : nullptr, s_ids, s_w, reinterpret_cast<uint32_t *>(ring),
-                                s_act + warp * k, s_ranked + warp);
+                                s_act + warp * k, s_ranked + warp, lbar);
         } else {
             dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
             named_barrier_arrive(kBarXReady, NTH);        // the routing warps sync on it later
@@ -321,7 +323,8 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
             int32_t *ids = lead ? a.topk_ids : nullptr;
             float *w = lead ? a.topk_w : nullptr;
             // keys in this warp's task ring, which no copy has touched yet
-            route_token_compact(row, a.E, k, warp, ids, w, s_ids, s_w, reinterpret_cast<uint32_t *>(ring));
+            route_token_compact(row, a.E, k, warp, ids, w, s_ids, s_w, reinterpret_cast<uint32_t *>(ring), nullptr,
+                                nullptr, lbar);
         } else if (NTH > 32 * a.T) {  // the host keeps NW > T
             dec_stage_rows(a.x, a.T, H, G1, cache, tid - 32 * a.T, NTH - 32 * a.T);
         }
@@ -621,11 +624,22 @@ __global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) decode_layer_kernel(co
         }
         // out[t][n] = sum_j w[t][j] y[t*k+j][n]: lanes (o, js) sum j = js, js+4, ...,
         // then a fixed shuffle tree over js (deterministic order)
+        // (every load of a lane issued before the first product: one L2
+        // round trip instead of one per term)
         const int n = nb * 8 + o;
         float accv = 0.f;
-        for (int j = js; j < k; j += 4) {
-            const int p = t * k + j;
-            accv = fmaf(s_w[p], __ldcg(a.y + (size_t)p * H + n), accv);
+        for (int j0 = js; j0 < k; j0 += 32) {
+            float yv[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + 4 * jj;
+                yv[jj] = j < k ? __ldcg(a.y + (size_t)(t * k + j) * H + n) : 0.f;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + 4 * jj;
+                if (j < k) accv = fmaf(s_w[t * k + j], yv[jj], accv);
+            }
         }
         accv += __shfl_xor_sync(0xffffffffu, accv, 8);
         accv += __shfl_xor_sync(0xffffffffu, accv, 16);
@@ -663,10 +677,8 @@ cudaError_t launch_layer_k(K kern, int *configured, const LayerArgs &a, const La
                            cudaStream_t stream) {
     cudaError_t e = ensure_smem(kern, configured, pl.smem);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, pl.nw * 32, pl.smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    // the cooperative launch itself fails (cudaErrorCooperativeLaunchTooLarge)
+    // unless every CTA can be resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(pl.nw * 32);

@@ -100,22 +100,51 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int E
 // kernel that routes once per launch runs this code once, and each 128-byte
 // line of straight-line code costs an L2 round trip on first use, so the
 // selection is a short loop over keys kept in shared memory (s_key: E
-// words of this warp) instead of unrolled register code.  Each of the k
-// rounds scans the lane's keys in ascending expert order (first maximum =
-// lowest index), takes the warp maximum and, among lanes holding it, the
-// lowest expert index; the winner's key is cleared.  Results are identical
-// to route_token's.  E <= 1024.  With pub_n, every round also publishes its
+// words of this warp) instead of unrolled register code.  Every lane keeps
+// the best of its keys (scanned in ascending expert order: first maximum =
+// lowest index); each of the k rounds takes the warp maximum and, among
+// lanes holding it, the lowest expert index, clears the winner's key, and
+// only the winning lane scans its keys again.  Results are identical to
+// route_token's.  E <= 1024.  With pub_n, every round also publishes its
 // winner at once: pub_id[s] = expert of rank s, then (after a block-scope
 // fence) *pub_n = s + 1, so other warps of the CTA can act on the first
 // ranks while the later ones are still being chosen.
+//
+// With lbar (an mbarrier of this warp's own, in shared memory), a row that
+// starts on a 16-byte boundary with E a multiple of 4 arrives by one bulk
+// copy into s_key and is turned into keys in place by a short loop: the
+// straight-line code of 32 loads per lane is the longest stretch of cold
+// code in a kernel that routes once.  The winners' logits are recovered
+// from their keys (order_key is invertible up to -0 -> +0 and the NaN
+// payload), so the row is read once.
+__device__ __forceinline__ float key_value(uint32_t key) {
+    const uint32_t u = key - 1u;
+    return __uint_as_float((u & 0x80000000u) ? (u ^ 0x80000000u) : ~u);
+}
+
 template <bool FRESH = false>
 __device__ __forceinline__ void route_token_compact(const float *__restrict__ row, int E, int k, int t,
                                                     int32_t *__restrict__ topk_ids,
                                                     float *__restrict__ topk_w, int *s_ids, float *s_w,
                                                     uint32_t *s_key, int *pub_id = nullptr,
-                                                    volatile int *pub_n = nullptr) {
+                                                    volatile int *pub_n = nullptr, uint64_t *lbar = nullptr) {
     const int lane = threadIdx.x & 31;
-    {
+    bool loaded = false;
+    if (lbar && ((reinterpret_cast<uintptr_t>(row) | (uintptr_t)E * 4u) & 15u) == 0) {
+        if (lane == 0) {
+            mbar_init(lbar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(lbar, (uint32_t)E * 4u);
+            bulk_g2s(s_key, row, (uint32_t)E * 4u, lbar);
+        }
+        __syncwarp();
+        // a wait that expires (about a second; never with a working copy
+        // engine) falls back to the loads below
+        loaded = mbar_wait_bounded(lbar, 0, nullptr);
+        if (loaded)
+            for (int e = lane; e < E; e += 32) s_key[e] = order_key(__uint_as_float(s_key[e]));
+    }
+    if (!loaded) {
         // every load first (one memory round trip), then the keys
         float v[32];
 #pragma unroll
@@ -125,32 +154,49 @@ __device__ __forceinline__ void route_token_compact(const float *__restrict__ ro
             if (lane + 32 * j < E) s_key[lane + 32 * j] = order_key(v[j]);
     }
     __syncwarp();
-    int my_id = 0;
-    for (int s = 0; s < k; ++s) {
-        // two interleaved scans (even and odd strides), merged keeping the lower index on ties
-        uint32_t b0 = 0, b1 = 0;
-        int e0 = 0x7fffffff, e1 = 0x7fffffff;
-        for (int e = lane; e < E; e += 64) {
-            const uint32_t v0 = s_key[e];
-            if (v0 > b0) { b0 = v0; e0 = e; }
-            if (e + 32 < E) {
-                const uint32_t v1 = s_key[e + 32];
-                if (v1 > b1) { b1 = v1; e1 = e + 32; }
+    // each lane's best untaken key and its expert (the first maximum in
+    // ascending expert order, so the lowest index among equal keys); only the
+    // lane whose candidate a round takes scans its keys again
+    uint32_t bk = 0;
+    int be = 0x7fffffff;
+    auto lane_scan = [&]() {
+        bk = 0;
+        be = 0x7fffffff;
+        for (int e0 = lane; e0 < E; e0 += 256) {
+            uint32_t v[8];  // eight loads in flight, then the compares in ascending order
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = e0 + 32 * u < E ? s_key[e0 + 32 * u] : 0u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (v[u] > bk) {
+                    bk = v[u];
+                    be = e0 + 32 * u;
+                }
             }
         }
-        if (b1 > b0 || (b1 == b0 && e1 < e0)) { b0 = b1; e0 = e1; }
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, b0);
-        const int win = (int)__reduce_min_sync(0xffffffffu, b0 == kmax ? (uint32_t)e0 : 0xffffffffu);
-        if (lane == s) my_id = win;
-        if (lane == (win & 31)) s_key[win] = 0u;
+    };
+    lane_scan();
+    int my_id = 0;
+    uint32_t my_key = 0;
+    for (int s = 0; s < k; ++s) {
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const int win = (int)__reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)be : 0xffffffffu);
+        if (lane == s) {
+            my_id = win;
+            my_key = kmax;
+        }
         if (pub_n && lane == 0) {
             pub_id[s] = win;
             __threadfence_block();
             *pub_n = s + 1;
         }
+        if (lane == (win & 31)) {
+            s_key[win] = 0u;
+            lane_scan();
+        }
         __syncwarp();
     }
-    const float my_logit = lane < k ? load_logit<FRESH>(row + my_id) : 0.f;
+    const float my_logit = lane < k ? key_value(my_key) : 0.f;
     const float m = __shfl_sync(0xffffffffu, my_logit, 0);
     const float ex = (lane < k) ? expf(my_logit - m) : 0.f;
     float sum = ex;
