@@ -542,6 +542,29 @@ def per_config_figures(moe, dev, geoms, names, sets: int, fmt: str = "w4a16"):
     return out
 
 
+def launch_floor(moe, rig, T, E, k, H, I, n: int):
+    """µs of the empty kernel launched with the one-call layer's launch shape
+    (moe_decode_layer_floor), back to back and each alone, timed as the
+    layer is; None where the shape does not take the one-launch path."""
+    import ctypes
+    import torch
+    if T > 8 or moe.moe_decode_layer_floor(T, E, k, H, I, rig.stream, check=False) != moe.MOE_OK:
+        return None
+    f = moe.load_library().moe_decode_layer_floor
+    sp = ctypes.c_void_p(rig.stream.cuda_stream)
+    call = lambda s: f(T, E, k, H, I, sp)
+    iso = rig.timed(n, 0, call)
+    torch.cuda._sleep(2000000)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(rig.stream)
+    for j in range(n):
+        call(j)
+    e1.record(rig.stream)
+    torch.cuda.synchronize()
+    return {"back_to_back": e0.elapsed_time(e1) / n * 1e3, "isolated_median": float(np.median(iso) * 1e3),
+            "launches": 2 * n, "what": "empty kernel, the layer's grid, block, shared memory and cooperative launch"}
+
+
 # grouped by weight geometry, so each geometry's weights are generated once
 TIMELINE_PHASES = ("entry", "routed_and_grouped", "first_copies_issued", "first_stage_landed",
                    "gate_up_done", "down_inputs_ready", "down_done", "exit")
@@ -845,6 +868,7 @@ def main():
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in e2e_ev), dev)
         e2e_val = whole_job_rate(world, T, e2e_steps, e2e_ms)
+        floor = launch_floor(moe, rig, T, E, k, H, I, n2)
         timeline = None
         if args.timeline > 0 and T <= 8:
             timeline = phase_timeline(moe, rig, args.timeline, dev)
@@ -907,6 +931,7 @@ def main():
             "mid_size": mid,
             "around_layer": around,
             "timeline": timeline,
+            "launch_floor_us": floor,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": T * E * 4 + T * H * 2,

@@ -234,6 +234,16 @@ int moe_w4a16_down_combine(const uint16_t *h,
  * input. */
 size_t moe_layer_workspace_bytes(int T, int E, int k, int H, int I);
 
+/* Diagnostic, the launch-cost floor of the call above: launches an empty
+ * kernel exactly as moe_w4a16_moe_layer launches its one cooperative
+ * kernel for this shape (grid = one CTA per SM, the same block size and
+ * dynamic shared memory, cooperative), on `stream`, and computes nothing.
+ * The layer's time minus this one is what its kernel costs beyond
+ * launching.  MOE_ERR_UNSUPPORTED where the shape does not take the
+ * one-launch path; MOE_OK for T == 0 (nothing launched); MOE_ERR_CUDA on a
+ * launch error.  Takes no buffers. */
+int moe_decode_layer_floor(int T, int E, int k, int H, int I, void *stream);
+
 int moe_w4a16_moe_layer(const float *logits, const uint16_t *x,
                         const uint32_t *w13_q, const uint16_t *w13_s, const uint32_t *w13_z,
                         const uint32_t *w2_q, const uint16_t *w2_s, const uint32_t *w2_z,

@@ -122,6 +122,9 @@ def test_new_calls_validate_before_the_device(lib):
                                       None) == moe.MOE_ERR_WORKSPACE
     assert lib.moe_router_route_align(p, p, 4, 2048, 2, 256, p, p, p, p, p, p, p, p, 512,
                                       None) == moe.MOE_ERR_UNSUPPORTED                  # E > 1024
+    # launch floor: the layer's size checks
+    assert lib.moe_decode_layer_floor(1, 0, 10, 2560, 640, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_layer_floor(1, 512, 10, 2500, 640, None) == moe.MOE_ERR_INVALID_ARG
     # AWQ import: misplaced rows, K % 32, group size, overflowing destination
     imp = lambda E, K, N, g, Nd, r0: lib.moe_awq_import(p, p, p, E, K, N, g, p, p, p, Nd, r0, None)
     assert imp(1, 64, 16, 32, 32, 4) == moe.MOE_ERR_INVALID_ARG

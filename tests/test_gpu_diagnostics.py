@@ -90,3 +90,18 @@ def test_phase_timeline_is_filled_in_order(moe):
     assert np.all(entry > 0) and np.all(grouped >= entry) and np.all(exitt >= grouped)
     assert (exitt.max() - entry.min()) < 10_000_000   # one launch, well under 10 ms
     moe.set_diagnostics(layer.workspace)
+
+
+def test_launch_floor_runs_where_the_one_launch_layer_does(moe):
+    """The empty kernel with the layer's launch shape launches for decode
+    shapes, is refused where the layer runs its four steps, and leaves the
+    stream usable."""
+    assert moe.moe_decode_layer_floor(1, 512, 10, 2560, 640) == moe.MOE_OK
+    assert moe.moe_decode_layer_floor(4, SHAPE.E, SHAPE.k, SHAPE.H, SHAPE.I) == moe.MOE_OK
+    assert moe.moe_decode_layer_floor(0, 512, 10, 2560, 640) == moe.MOE_OK
+    assert moe.moe_decode_layer_floor(64, 512, 10, 2560, 640, check=False) == moe.MOE_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    layer, logits, x, w13, w2 = _layer(moe, SHAPE)
+    out = layer.forward_layer(torch.from_numpy(logits).cuda(), torch.from_numpy(x).cuda()).float().cpu().numpy()
+    assert moe.moe_get_device_error(layer.workspace) == 0
+    assert _close(out, oracle.moe_forward(logits, x, w13, w2, SHAPE.k)["out"])

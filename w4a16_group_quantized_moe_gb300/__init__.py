@@ -46,7 +46,7 @@ EXPORTED = ("moe_abi_version", "moe_status_string", "moe_workspace_bytes", "moe_
             "moe_w4a16_down_combine_noalloc", "moe_layer_workspace_bytes", "moe_w4a16_moe_layer",
             "moe_nvfp4_gate_up_silu", "moe_nvfp4_down_combine", "moe_nvfp4_moe_layer",
             "moe_router_logits", "moe_router_route_align", "moe_awq_import",
-            "moe_w4a16_gate_up_silu_ex", "moe_w4a16_down_combine_ex")
+            "moe_w4a16_gate_up_silu_ex", "moe_w4a16_down_combine_ex", "moe_decode_layer_floor")
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +102,8 @@ def load_library(path: str = LIB_PATH):
         lib.moe_w4a16_down_combine_noalloc.restype = _I
         lib.moe_w4a16_down_combine_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                        _I, _I, _I, _I, _I, _P, _P]
+        lib.moe_decode_layer_floor.restype = _I
+        lib.moe_decode_layer_floor.argtypes = [_I, _I, _I, _I, _I, _P]
         lib.moe_layer_workspace_bytes.restype = _SZ
         lib.moe_layer_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
         lib.moe_w4a16_moe_layer.restype = _I
@@ -196,6 +198,15 @@ def set_diagnostics(workspace, wait_polls: int = 0, wait_extra: int = 0, timelin
 def moe_step_kernel_path(T: int, E: int, k: int, H: int, I: int) -> int:
     """MOE_PATH_* of the kernels the step calls run for this shape."""
     return int(load_library().moe_step_kernel_path(T, E, k, H, I))
+
+
+def moe_decode_layer_floor(T: int, E: int, k: int, H: int, I: int, stream=None, check: bool = True) -> int:
+    """Launches the empty kernel with the one-call layer's launch shape (the
+    launch-cost floor); returns the status (raises unless OK when check)."""
+    st = int(load_library().moe_decode_layer_floor(T, E, k, H, I, _stream(stream)))
+    if check:
+        _check("moe_decode_layer_floor", st)
+    return st
 
 
 def moe_get_device_error(workspace, stream=None) -> int:

@@ -62,6 +62,7 @@ cudaError_t launch_gate_up_tc_nvfp4(const __half *, const uint32_t *, const uint
 cudaError_t launch_down_tc_nvfp4(const __half *, const uint32_t *, const uint8_t *, const float *,
                                  const int32_t *, const int32_t *, const int32_t *, const int32_t *, const float *,
                                  int, int, int, int, int, __half *, float *, uint32_t *, int, size_t, cudaStream_t);
+cudaError_t launch_layer_floor(int, int, int, int, int, int, size_t, cudaStream_t);
 cudaError_t launch_decode_layer_nvfp4(const float *, const __half *, const uint32_t *, const uint8_t *,
                                       const float *, const uint32_t *, const uint8_t *, const float *, int, int,
                                       int, int, int, int32_t *, float *, __half *, __half *, float *, uint32_t *,
@@ -445,6 +446,16 @@ LayerWorkspace layer_workspace(int T, int E, int k, int H, int I) {
 MOE_EXPORT size_t moe_layer_workspace_bytes(int T, int E, int k, int H, int I) {
     if (check_sizes(T, E, k, H, I) != MOE_OK) return 0;
     return layer_workspace(T, E, k, H, I).total;
+}
+
+MOE_EXPORT int moe_decode_layer_floor(int T, int E, int k, int H, int I, void *stream) {
+    int st = check_sizes(T, E, k, H, I);
+    if (st != MOE_OK) return st;
+    if (T == 0) return MOE_OK;
+    DeviceInfo di;
+    if (device_info(&di) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!layer_fusable(T, E, k, H, I, di.sms, di.smem_optin)) return MOE_ERR_UNSUPPORTED;
+    return cuda_status(launch_layer_floor(T, E, k, H, I, di.sms, di.smem_optin, static_cast<cudaStream_t>(stream)));
 }
 
 MOE_EXPORT int moe_w4a16_moe_layer(const float *logits, const uint16_t *x, const uint32_t *w13_q,

@@ -72,6 +72,32 @@ bool layer_fusable(int T, int E, int k, int H, int I, int num_sms, size_t smem_l
     return layer_plan(T, E, k, H, I, num_sms, smem_limit).ok;
 }
 
+// An empty kernel launched exactly as the layer kernel is for the same
+// shape (one CTA per SM, the plan's warps and dynamic shared memory, a
+// cooperative launch): the cost of the launch alone, the floor under the
+// layer's time.
+__global__ void __launch_bounds__(kLayerMaxWarps * 32, 1) layer_floor_kernel() {}
+
+cudaError_t launch_layer_floor(int T, int E, int k, int H, int I, int num_sms, size_t smem_limit,
+                               cudaStream_t stream) {
+    const LayerPlan pl = layer_plan(T, E, k, H, I, num_sms, smem_limit);
+    if (!pl.ok) return cudaErrorInvalidConfiguration;
+    static int configured[128];
+    cudaError_t e = ensure_smem(layer_floor_kernel, configured, pl.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(pl.nw * 32);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, layer_floor_kernel);
+}
+
 template <int FMT>
 static cudaError_t launch_decode_layer_f(const float *logits, const __half *x, const uint32_t *q13,
                                          const __half *s13, const uint32_t *z13, const uint32_t *q2,
