@@ -30,10 +30,10 @@ LayerPlan layer_plan(int T, int E, int k, int H, int I, int num_sms, size_t smem
     // the router keeps E keys in a routing warp's ring before any copy
     if ((size_t)kLayerSlots * pl.slot_bytes < (size_t)E * 4) pl.slot_bytes = (uint32_t)align_up((size_t)E * 4 / kLayerSlots, 128);
     // h rows one CTA's down share can read.  Shares are contiguous runs of
-    // tasks of equal weight, a task of expert a weighing (2 + rows of a), so
-    // the experts wholly inside a share hold at most 3P/NC + 1 rows; the two
-    // experts cut by its ends add at most T rows each.
-    const long long hr = (3LL * P + num_sms - 1) / num_sms + 1 + 2LL * T;
+    // tasks of equal weight, a task of expert a weighing (1 + rows of a), so
+    // the experts wholly inside a share hold at most (A + P)/NC + 1 <=
+    // 2P/NC + 1 rows; the two experts cut by its ends add at most T rows each.
+    const long long hr = (2LL * P + num_sms - 1) / num_sms + 1 + 2LL * T;
     pl.hrows = (int)(hr < P ? hr : P);
     for (int nw = kLayerMaxWarps; nw >= kLayerMinWarps; --nw) {
         if (nw <= T) break;  // warps beyond the T routing warps stage x
